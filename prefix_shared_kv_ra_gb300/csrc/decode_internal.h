@@ -1,0 +1,70 @@
+// decode_internal.h -- parameter blocks shared by the decode kernels and the
+// tensor-core prefix pass of the cascade (grouped) decode.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cmath>
+
+#include "../../include/ra.h"
+
+namespace ra {
+
+struct DecodeParams {
+  const __nv_bfloat16* k_pool;
+  const __nv_bfloat16* v_pool;
+  int64_t num_slots;
+  int32_t hkv;
+  const __nv_bfloat16* q;  // [batch, hq, D]
+  __nv_bfloat16* o;        // [batch, hq, D]
+  int32_t hq;
+  int32_t group;     // hq / hkv
+  float scale_log2;  // sm_scale * log2(e)
+  const int32_t* table;
+  int64_t table_stride;
+  int64_t table_rows;
+  const int32_t* rpi;
+  const int32_t* seq_lens;
+  int32_t batch;
+  int32_t max_seq_len;
+  const int32_t* key_start;  // [batch] first private position (cascade), or nullptr
+  int32_t chunk;             // keys per split
+  int32_t max_splits;
+  float* part_o;    // [batch, hq, max_splits, D]
+  float* part_lse;  // [batch, hq, max_splits] (log2 domain)
+  float* casc_o;    // [batch, hq, D] shared-prefix partial (cascade)
+  float* casc_lse;  // [batch, hq]
+  uint32_t* err;
+};
+
+struct DecodePlan {
+  int32_t chunk = 0;
+  int32_t max_splits = 0;
+};
+
+struct DecodeWorkspace {
+  size_t part_o = 0, part_lse = 0, casc_o = 0, casc_lse = 0, key_start = 0, total = 0;
+};
+
+struct CascadeArgs {
+  const int32_t* group_indptr;
+  const int32_t* group_reqs;
+  const int32_t* group_prefix_len;
+  int32_t num_groups;
+  int32_t max_group_prefix_len;
+  int32_t max_group_size;
+};
+
+DecodePlan plan_decode(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len);
+DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int32_t head_dim,
+                                        const DecodePlan& pl, bool cascade);
+
+// Tensor-core pass over each group's shared prefix: writes p.casc_o / p.casc_lse
+// for every member (defined with the tcgen05 attention kernel).
+ra_status launch_cascade_prefix(const DecodeParams& p, const CascadeArgs& ca, int32_t head_dim,
+                                cudaStream_t stream);
+
+}  // namespace ra

@@ -1,0 +1,109 @@
+"""Shared helpers for the GPU parity tests: move a generator batch to the
+device, run the hot path through the Python binding, compare with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import prefix_shared_kv_ra_gb300 as ra
+import workloads as W
+
+ATOL = 1e-2
+RTOL = 1e-2
+
+
+def bf16(a: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def i32(a: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+class DeviceBatch:
+    """A generator batch resident on the GPU (pool before the store)."""
+
+    def __init__(self, b: W.Batch, dev="cuda:0"):
+        self.b = b
+        self.dev = torch.device(dev)
+        S, hkv, d = b.num_slots, b.num_kv_heads, b.head_dim
+        self.k_pool = torch.zeros((S, hkv, d), dtype=torch.bfloat16, device=self.dev)
+        self.v_pool = torch.zeros((S, hkv, d), dtype=torch.bfloat16, device=self.dev)
+        if b.pool_slots.size:
+            idx = torch.from_numpy(b.pool_slots.astype(np.int64)).to(self.dev)
+            self.k_pool.index_copy_(0, idx, bf16(b.pool_k, self.dev))
+            self.v_pool.index_copy_(0, idx, bf16(b.pool_v, self.dev))
+        self.k_new = bf16(b.k_new, self.dev)
+        self.v_new = bf16(b.v_new, self.dev)
+        self.loc = i32(b.out_cache_loc, self.dev)
+        self.table = i32(b.req_to_token, self.dev)
+        self.ext_q = bf16(b.ext_q, self.dev)
+        self.ext_rpi = i32(b.ext_rpi, self.dev)
+        self.ext_prefix = i32(b.ext_prefix_lens, self.dev)
+        self.ext_len = i32(b.ext_extend_lens, self.dev)
+        self.ext_qo = i32(b.ext_qo_indptr, self.dev)
+        self.dec_q = bf16(b.dec_q, self.dev)
+        self.dec_rpi = i32(b.dec_rpi, self.dev)
+        self.dec_lens = i32(b.dec_seq_lens, self.dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=self.dev)
+        if b.has_cascade():
+            self.g_indptr = i32(b.casc_group_indptr, self.dev)
+            self.g_reqs = i32(b.casc_group_reqs, self.dev)
+            self.g_plen = i32(b.casc_group_prefix_len, self.dev)
+        self.ext_o = torch.empty_like(self.ext_q)
+        self.dec_o = torch.empty_like(self.dec_q)
+        self.ws = torch.empty(0, dtype=torch.uint8, device=self.dev)
+
+    # -- the three calls
+    def store(self):
+        ra.ra_kv_store(self.k_pool, self.v_pool, self.k_new, self.v_new, self.loc, device_error=self.err)
+
+    def extend(self):
+        b = self.b
+        if b.n_extend == 0:
+            return
+        ra.ra_extend_attention(self.k_pool, self.v_pool, self.ext_q, self.ext_o, self.table, self.ext_rpi,
+                               self.ext_prefix, self.ext_len, self.ext_qo, max_extend_len=b.max_extend_len,
+                               max_prefix_len=b.max_prefix_len, sm_scale=b.sm_scale, device_error=self.err)
+
+    def decode_ws(self, cascade: bool) -> torch.Tensor:
+        b = self.b
+        ng, mp, ms = 0, 0, 0
+        if cascade:
+            ng = b.casc_group_indptr.size - 1
+            mp = int(b.casc_group_prefix_len.max())
+            ms = int(np.diff(b.casc_group_indptr).max())
+        n = ra.ra_decode_workspace_bytes(b.n_decode, b.num_q_heads, b.num_kv_heads, b.head_dim, b.max_seq_len,
+                                         ng, mp, ms)
+        if self.ws.numel() < n:
+            self.ws = torch.empty(n, dtype=torch.uint8, device=self.dev)
+        return self.ws
+
+    def decode(self, cascade: bool = False):
+        b = self.b
+        if b.n_decode == 0:
+            return
+        ws = self.decode_ws(cascade)
+        kw = {}
+        if cascade:
+            kw = dict(group_indptr=self.g_indptr, group_reqs=self.g_reqs, group_prefix_len=self.g_plen,
+                      max_group_prefix_len=int(b.casc_group_prefix_len.max()),
+                      max_group_size=int(np.diff(b.casc_group_indptr).max()))
+        ra.ra_decode_attention(self.k_pool, self.v_pool, self.dec_q, self.dec_o, self.table, self.dec_rpi,
+                               self.dec_lens, max_seq_len=b.max_seq_len, sm_scale=b.sm_scale, workspace=ws,
+                               device_error=self.err, **kw)
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, what: str):
+    err = np.abs(got - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = err > bound
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} elements outside 1e-2 + 1e-2|ref| "
+                             f"(max err {err.max():.3e}; first at {tuple(i)}: got {got[tuple(i)]}, "
+                             f"ref {ref[tuple(i)]})")

@@ -1,0 +1,97 @@
+"""The C-ABI library: it loads, exports every symbol include/ra.h declares, and its
+host-side validation rejects bad arguments before touching a GPU (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import prefix_shared_kv_ra_gb300 as ra
+from prefix_shared_kv_ra_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return ra.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "ra.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ra_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("ra_kv_store", "ra_extend_attention", "ra_decode_attention", "ra_decode_workspace_bytes",
+              "ra_status_string", "ra_last_error_message", "ra_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (ra_[a-z0-9_]+)\b", out))
+    missing = [n for n in _declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in _declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_abi_version_and_status_strings(lib):
+    assert ra.ra_abi_version() == 1
+    assert lib.ra_status_string(0) == b"ok"
+    assert lib.ra_status_string(3) == b"workspace too small"
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+
+
+def _decode_call(lib, **over):
+    args = dict(k=FAKE, v=FAKE, S=1024, hkv=8, d=128, q=FAKE, o=FAKE, hq=32, scale=0.088, table=FAKE,
+                stride=4096, rows=64, rpi=FAKE, lens=FAKE, batch=4, max_len=4096, ng=0, gi=None, gr=None, gp=None,
+                mgp=0, mgs=0, ws=FAKE, wsb=1 << 30, err=None, stream=None)
+    args.update(over)
+    return lib.ra_decode_attention(*args.values())
+
+
+def test_decode_validation(lib):
+    assert _decode_call(lib, hq=30) == 1                       # Hq % Hkv != 0
+    assert _decode_call(lib, d=96) == 2                        # unsupported head_dim
+    assert _decode_call(lib, hq=128) == 2                      # group 16 > 8
+    assert _decode_call(lib, wsb=16) == 3                      # workspace too small
+    assert b"workspace" in lib.ra_last_error_message()
+    assert _decode_call(lib, q=ctypes.c_void_p((1 << 20) + 8)) == 1   # misaligned q
+    assert _decode_call(lib, stride=100) == 1                  # table narrower than max_seq_len
+    assert _decode_call(lib, scale=float("nan")) == 1
+    assert _decode_call(lib, batch=-1) == 1
+    assert _decode_call(lib, ng=2, gi=None) == 1               # cascade arrays missing
+    assert _decode_call(lib, batch=0) == 0                     # empty batch: no-op
+
+
+def test_decode_workspace_grows_with_bounds(lib):
+    a = ra.ra_decode_workspace_bytes(64, 32, 8, 128, 4096)
+    b = ra.ra_decode_workspace_bytes(64, 32, 8, 128, 8192)
+    c = ra.ra_decode_workspace_bytes(64, 32, 8, 128, 4096, 8, 1024, 8)
+    assert 0 < a < b and c > a
+    assert ra.ra_decode_workspace_bytes(0, 32, 8, 128, 4096) == 0
+
+
+def test_kv_store_validation(lib):
+    f = lib.ra_kv_store
+    assert f(FAKE, FAKE, 16, 8, 128, FAKE, FAKE, FAKE, 0, None, None) == 0        # zero tokens: no-op
+    assert f(FAKE, FAKE, 16, 8, 128, FAKE, FAKE, FAKE, -1, None, None) == 1
+    assert f(FAKE, FAKE, 16, 1, 4, FAKE, FAKE, FAKE, 3, None, None) == 1         # 8-byte rows
+    assert f(None, FAKE, 16, 8, 128, FAKE, FAKE, FAKE, 3, None, None) == 1
+    assert f(ctypes.c_void_p((1 << 20) + 4), FAKE, 16, 8, 128, FAKE, FAKE, FAKE, 3, None, None) == 1
+
+
+def test_binding_refuses_to_run_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(ra, "_lib", None)
+    monkeypatch.setattr(_build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        ra.load()

@@ -1,0 +1,157 @@
+"""GPU parity: KV store (bit-exact) and decode attention (1e-2 abs + 1e-2 rel) against
+the CPU oracle, through the C ABI, on small ragged cases and the full workloads."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import prefix_shared_kv_ra_gb300 as ra
+import workloads as W
+from helpers import DeviceBatch, assert_close, bf16, i32, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _pool_rows(t: torch.Tensor, slots: np.ndarray) -> np.ndarray:
+    idx = torch.from_numpy(slots.astype(np.int64)).to(t.device)
+    return t.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def check_store(db: DeviceBatch, n_other: int = 256):
+    b = db.b
+    db.store()
+    torch.cuda.synchronize()
+    assert int(db.err.item()) == 0
+    rng = np.random.default_rng(0)
+    untouched = np.setdiff1d(rng.integers(0, b.num_slots, size=n_other), b.out_cache_loc)
+    sample = np.concatenate([b.out_cache_loc.astype(np.int64), untouched])
+    # oracle store on the sampled slots (the store commutes with relabelling slots)
+    before_k = np.zeros((sample.size, b.num_kv_heads, b.head_dim), np.uint16)
+    before_v = np.zeros_like(before_k)
+    pos = {s: i for i, s in enumerate(b.pool_slots.tolist())}
+    for j, s in enumerate(sample.tolist()):
+        if s in pos:
+            before_k[j] = b.pool_k[pos[s]]
+            before_v[j] = b.pool_v[pos[s]]
+    local = np.arange(b.out_cache_loc.size, dtype=np.int32)
+    exp_k, exp_v = oracle.kv_store(before_k, before_v, b.k_new, b.v_new, local)
+    np.testing.assert_array_equal(_pool_rows(db.k_pool, sample), exp_k)
+    np.testing.assert_array_equal(_pool_rows(db.v_pool, sample), exp_v)
+
+
+def check_decode(db: DeviceBatch, sel=None, cascade=False):
+    b = db.b
+    db.decode(cascade=cascade)
+    torch.cuda.synchronize()
+    assert int(db.err.item()) == 0
+    got = to_f64(db.dec_o).reshape(-1, b.head_dim)
+    ref = oracle.decode_batch(b, sel=sel)
+    if sel is not None:
+        got = got[sel]
+    assert_close(got, ref, f"{b.name} decode")
+
+
+# ---------------------------------------------------------------- store
+def test_store_tiny_bit_exact():
+    e, d = W.cfg1_tiny()
+    for b in (e, d):
+        db = DeviceBatch(b)
+        db.store()
+        torch.cuda.synchronize()
+        k_ref, v_ref = oracle.kv_store(*b.dense_pool(), b.k_new, b.v_new, b.out_cache_loc)
+        got_k = db.k_pool.view(torch.int16).cpu().numpy().view(np.uint16)
+        got_v = db.v_pool.view(torch.int16).cpu().numpy().view(np.uint16)
+        np.testing.assert_array_equal(got_k, k_ref)   # the whole pool, bit for bit
+        np.testing.assert_array_equal(got_v, v_ref)
+
+
+@pytest.mark.parametrize("name", ["cfg2_decode_8b", "cfg3_fewshot_extend", "cfg4_forked_decode_70b",
+                                  "cfg5_multiturn_mix_70b"])
+def test_store_full_workloads(name):
+    check_store(DeviceBatch(W.CONFIGS[name]()))
+
+
+def test_store_empty_and_bad_slot_flag():
+    b = W.random_mixed(3, n_extend=1, n_decode=3, num_q_heads=4, num_kv_heads=2, head_dim=64, max_len=20)
+    db = DeviceBatch(b)
+    ra.ra_kv_store(db.k_pool, db.v_pool, db.k_new[:0], db.v_new[:0], db.loc[:0], device_error=db.err)
+    bad = db.loc.clone()
+    bad[0] = b.num_slots + 5
+    before = db.k_pool.clone()
+    ra.ra_kv_store(db.k_pool, db.v_pool, db.k_new, db.v_new, bad, device_error=db.err)
+    torch.cuda.synchronize()
+    assert int(db.err.item()) & ra.DEVERR_SLOT
+    # the bad row is skipped, the others written
+    assert torch.equal(db.k_pool[b.out_cache_loc[1]], db.k_new[1])
+    changed = (db.k_pool != before).any(dim=(1, 2)).nonzero().flatten().cpu().numpy()
+    assert set(changed.tolist()) <= set(b.out_cache_loc[1:].tolist())
+
+
+# ---------------------------------------------------------------- decode
+def test_decode_tiny_config():
+    _, d = W.cfg1_tiny()
+    db = DeviceBatch(d)
+    db.store()
+    check_decode(db)
+
+
+@pytest.mark.parametrize("seed,hq,hkv,d,max_len", [
+    (0, 8, 2, 64, 40), (1, 32, 8, 128, 700), (2, 16, 2, 128, 1500), (3, 8, 8, 128, 300),
+    (4, 4, 2, 64, 2600), (5, 64, 8, 128, 1200), (6, 6, 3, 128, 260)])
+def test_decode_ragged(seed, hq, hkv, d, max_len):
+    b = W.random_mixed(seed, n_extend=0, n_decode=9, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                       max_len=max_len)
+    db = DeviceBatch(b)
+    db.store()
+    check_decode(db)
+
+
+def test_decode_single_token_contexts():
+    b = W.random_mixed(8, n_extend=0, n_decode=5, num_q_heads=8, num_kv_heads=2, head_dim=128, max_len=1,
+                       min_len=1, share_prob=0.0)
+    db = DeviceBatch(b)
+    db.store()
+    check_decode(db)
+    # one key: the output is that key's V row rounded to bf16
+    v = to_f64(db.v_new).reshape(5, 2, 128)
+    got = to_f64(db.dec_o).reshape(5, 8, 128)
+    np.testing.assert_array_equal(got, np.repeat(v, 4, axis=1))
+
+
+@pytest.mark.parametrize("name", ["cfg2_decode_8b", "cfg4_forked_decode_70b"])
+def test_decode_full_workloads(name):
+    b = W.CONFIGS[name]()
+    db = DeviceBatch(b)
+    db.store()
+    check_decode(db)
+
+
+def test_decode_multiturn_mix_sampled():
+    b = W.cfg5_multiturn_mix_70b()
+    db = DeviceBatch(b)
+    db.store()
+    rng = np.random.default_rng(1)
+    sel = np.sort(rng.choice(b.n_decode * b.num_q_heads, size=384, replace=False))
+    # always include the longest context
+    longest = int(np.argmax(b.dec_seq_lens))
+    sel = np.unique(np.concatenate([sel, longest * b.num_q_heads + np.arange(b.num_q_heads)]))
+    check_decode(db, sel=sel)
+
+
+def test_decode_bad_table_row_is_flagged_not_faulted():
+    b = W.random_mixed(9, n_extend=0, n_decode=4, num_q_heads=8, num_kv_heads=2, head_dim=64, max_len=50)
+    db = DeviceBatch(b)
+    db.store()
+    db.table[b.dec_rpi[1], 0] = -7           # a corrupt slot id
+    db.decode()
+    torch.cuda.synchronize()
+    assert int(db.err.item()) & ra.DEVERR_SLOT
+
+
+def test_decode_empty_batch_is_noop():
+    b = W.random_mixed(10, n_extend=0, n_decode=2, num_q_heads=8, num_kv_heads=2, head_dim=64, max_len=20)
+    db = DeviceBatch(b)
+    ws = torch.empty(1024, dtype=torch.uint8, device=db.dev)
+    ra.ra_decode_attention(db.k_pool, db.v_pool, db.dec_q[:0], db.dec_o[:0], db.table, db.dec_rpi[:0],
+                           db.dec_lens[:0], max_seq_len=b.max_seq_len, sm_scale=b.sm_scale, workspace=ws)
+    torch.cuda.synchronize()
