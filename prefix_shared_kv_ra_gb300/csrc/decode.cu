@@ -301,17 +301,21 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
   const bool has_prefix = start > 0;
   if (n_splits == 1 && !has_prefix) return;  // written directly by the split kernel
   const int64_t bh = warp_global;
-  float mm = has_prefix ? p.casc_lse[bh] : -INFINITY;
+  const int32_t n_pre = has_prefix ? (start + p.cchunk - 1) / p.cchunk : 0;  // prefix-pass splits
+  float mm = -INFINITY;
+  for (int s = 0; s < n_pre; ++s) mm = fmaxf(mm, p.casc_lse[bh * p.max_csplits + s]);
   for (int s = 0; s < n_splits; ++s) mm = fmaxf(mm, p.part_lse[bh * p.max_splits + s]);
   float acc[V];
   float wsum = 0.f;
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
-  if (has_prefix) {
-    const float w = ex2(p.casc_lse[bh] - mm);
+  for (int s = 0; s < n_pre; ++s) {
+    const int64_t ps = bh * p.max_csplits + s;
+    const float w = ex2(p.casc_lse[ps] - mm);
     wsum += w;
+    const float* src = p.casc_o + ps * D + lane * V;
 #pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] += w * p.casc_o[bh * D + lane * V + v];
+    for (int v = 0; v < V; ++v) acc[v] += w * src[v];
   }
   for (int s = 0; s < n_splits; ++s) {
     const int64_t ps = bh * p.max_splits + s;
@@ -374,8 +378,11 @@ ra_status launch_decode(const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-// Keys per split: at least 128, at most 1024, aiming at ~2K (request, kv head, split) work items.
-DecodePlan plan_decode(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len) {
+// Private keys per split: at least 128, at most 1024, aiming at ~2K (request, kv head, split) work items.
+// Shared-prefix pass (cascade): 128-row tiles of (member, q head) per group and kv head; the prefix is
+// split in multiples of 128 keys until there are about two CTAs per SM of work.
+DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seq_len,
+                       int32_t num_groups, int32_t max_group_prefix_len, int32_t max_group_size) {
   DecodePlan pl;
   const int64_t work = static_cast<int64_t>(batch) * num_kv_heads * (max_seq_len > 0 ? max_seq_len : 1);
   int64_t chunk = (work + 2047) / 2048;
@@ -385,6 +392,19 @@ DecodePlan plan_decode(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len)
   pl.chunk = static_cast<int32_t>(chunk);
   pl.max_splits = static_cast<int32_t>((static_cast<int64_t>(max_seq_len) + chunk - 1) / chunk);
   if (pl.max_splits < 1) pl.max_splits = 1;
+  if (num_groups > 0 && max_group_prefix_len > 0) {
+    const int32_t group = num_q_heads / num_kv_heads;
+    const int32_t rows_per_tile = 128 / (group > 0 ? group : 1);
+    const int64_t mtiles = (max_group_size + rows_per_tile - 1) / rows_per_tile;
+    const int64_t base = static_cast<int64_t>(num_groups) * num_kv_heads * mtiles;
+    const int64_t key_tiles = (max_group_prefix_len + 127) / 128;
+    int64_t want = (304 + base - 1) / base;
+    if (want < 1) want = 1;
+    if (want > key_tiles) want = key_tiles;
+    const int64_t tiles_per_split = (key_tiles + want - 1) / want;
+    pl.cchunk = static_cast<int32_t>(tiles_per_split * 128);
+    pl.max_csplits = static_cast<int32_t>((max_group_prefix_len + pl.cchunk - 1) / pl.cchunk);
+  }
   return pl;
 }
 
@@ -400,9 +420,9 @@ DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int3
   off += up(bh * pl.max_splits * sizeof(float));
   if (cascade) {
     w.casc_o = off;
-    off += up(bh * head_dim * sizeof(float));
+    off += up(bh * pl.max_csplits * head_dim * sizeof(float));
     w.casc_lse = off;
-    off += up(bh * sizeof(float));
+    off += up(bh * pl.max_csplits * sizeof(float));
     w.key_start = off;
     off += up(static_cast<size_t>(batch) * sizeof(int32_t));
   }
@@ -415,10 +435,10 @@ DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int3
 extern "C" size_t ra_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                             int32_t head_dim, int32_t max_seq_len, int32_t num_groups,
                                             int32_t max_group_prefix_len, int32_t max_group_size) {
-  (void)max_group_prefix_len;
-  (void)max_group_size;
   if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
-  const ra::DecodePlan pl = ra::plan_decode(batch, num_kv_heads, max_seq_len);
+  if (num_groups > 0 && (max_group_prefix_len <= 0 || max_group_size <= 0)) return 0;
+  const ra::DecodePlan pl = ra::plan_decode(batch, num_q_heads, num_kv_heads, max_seq_len, num_groups,
+                                            max_group_prefix_len, max_group_size);
   return ra::layout_decode_workspace(batch, num_q_heads, head_dim, pl, num_groups > 0).total;
 }
 
@@ -459,7 +479,8 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
                "max_group_prefix_len must be in [1, max_seq_len]");
     RA_REQUIRE(max_group_size >= 1 && max_group_size <= batch, "max_group_size must be in [1, batch]");
   }
-  const DecodePlan pl = plan_decode(batch, num_kv_heads, max_seq_len);
+  const DecodePlan pl = plan_decode(batch, num_q_heads, num_kv_heads, max_seq_len, num_groups,
+                                    max_group_prefix_len, max_group_size);
   const DecodeWorkspace wl = layout_decode_workspace(batch, num_q_heads, head_dim, pl, num_groups > 0);
   if (workspace_bytes < wl.total)
     return fail(RA_ERR_WORKSPACE, "workspace of %zu bytes, need %zu", workspace_bytes, wl.total);
@@ -491,6 +512,8 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   if (num_groups > 0) {
+    p.cchunk = pl.cchunk;
+    p.max_csplits = pl.max_csplits;
     p.casc_o = reinterpret_cast<float*>(ws + wl.casc_o);
     p.casc_lse = reinterpret_cast<float*>(ws + wl.casc_lse);
     int32_t* key_start = reinterpret_cast<int32_t*>(ws + wl.key_start);

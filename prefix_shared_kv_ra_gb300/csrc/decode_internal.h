@@ -35,14 +35,18 @@ struct DecodeParams {
   int32_t max_splits;
   float* part_o;    // [batch, hq, max_splits, D]
   float* part_lse;  // [batch, hq, max_splits] (log2 domain)
-  float* casc_o;    // [batch, hq, D] shared-prefix partial (cascade)
-  float* casc_lse;  // [batch, hq]
+  int32_t cchunk;      // shared-prefix keys per prefix-pass split (cascade)
+  int32_t max_csplits;  // prefix-pass splits per member
+  float* casc_o;        // [batch, hq, max_csplits, D] shared-prefix partials (cascade)
+  float* casc_lse;      // [batch, hq, max_csplits]
   uint32_t* err;
 };
 
 struct DecodePlan {
-  int32_t chunk = 0;
+  int32_t chunk = 0;        // private keys per split
   int32_t max_splits = 0;
+  int32_t cchunk = 0;       // shared-prefix keys per prefix-pass split (cascade)
+  int32_t max_csplits = 0;
 };
 
 struct DecodeWorkspace {
@@ -58,7 +62,8 @@ struct CascadeArgs {
   int32_t max_group_size;
 };
 
-DecodePlan plan_decode(int32_t batch, int32_t num_kv_heads, int32_t max_seq_len);
+DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seq_len,
+                       int32_t num_groups, int32_t max_group_prefix_len, int32_t max_group_size);
 DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int32_t head_dim,
                                         const DecodePlan& pl, bool cascade);
 

@@ -1,17 +1,194 @@
-// extend.cu -- placeholder until the tensor-core extend kernel lands.
+// extend.cu -- ra_extend_attention and the cascade prefix pass of
+// ra_decode_attention, both on the tcgen05 attention tile kernel.
+//
+// Extend is the dense contraction of this path: 128 query rows (128 / G
+// suffix tokens x the G q heads of one kv head) against 128-key tiles of the
+// request's context, QK^T and PV on the 5th-generation tensor cores with the
+// accumulators in TMEM.  Grid: (query tile, kv head, request); CTAs of one
+// (request, kv head) are adjacent so their shared prefix K/V tiles are served
+// from L2.
+// Sources: SGLang paper summary, §3 (reuse the cached prefix KV, compute
+// only the suffix); yaopepe.com explainer, §04 (the matched prefix is
+// referenced, the unmatched suffix is prefilled against it).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "api_common.h"
+#include "attn_tc.cuh"
 #include "decode_internal.h"
 
 namespace ra {
-ra_status launch_cascade_prefix(const DecodeParams&, const CascadeArgs&, int32_t, cudaStream_t) {
-  return fail(RA_ERR_UNSUPPORTED, "cascade decode not built yet");
+
+namespace {
+
+constexpr int kStages = 2;
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
 }
+
+template <typename Kern>
+ra_status set_smem(Kern kern, int bytes, bool* configured, int device) {
+  if (configured[device]) return RA_OK;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaFuncSetAttribute(attn_tc): %s", cudaGetErrorString(e));
+  configured[device] = true;
+  return RA_OK;
+}
+
+template <int D>
+ra_status launch_extend(const TcParams& p, const CUtensorMap& qmap, int max_tiles, int batch, cudaStream_t s) {
+  using L = tc::Layout<D, kStages>;
+  auto kern = attn_tc_kernel<D, kStages, true>;
+  static bool configured[64] = {};
+  DeviceInfo dev;
+  if (ra_status st = current_device(&dev)) return st;
+  if (L::kDynSmem > dev.max_smem_optin)
+    return fail(RA_ERR_UNSUPPORTED, "extend kernel needs %d bytes of shared memory", L::kDynSmem);
+  if (ra_status st = set_smem(kern, L::kDynSmem, configured, dev.device)) return st;
+  dim3 grid(max_tiles, p.hkv, batch);
+  kern<<<grid, tc::kThreads, L::kDynSmem, s>>>(p, qmap);
+  return check_launch("attn_tc_kernel<extend>");
+}
+
+template <int D>
+ra_status launch_prefix(const TcParams& p, int grid_x, int num_groups, cudaStream_t s) {
+  using L = tc::Layout<D, kStages>;
+  auto kern = attn_tc_kernel<D, kStages, false>;
+  static bool configured[64] = {};
+  DeviceInfo dev;
+  if (ra_status st = current_device(&dev)) return st;
+  if (L::kDynSmem > dev.max_smem_optin)
+    return fail(RA_ERR_UNSUPPORTED, "prefix kernel needs %d bytes of shared memory", L::kDynSmem);
+  if (ra_status st = set_smem(kern, L::kDynSmem, configured, dev.device)) return st;
+  CUtensorMap unused{};
+  dim3 grid(grid_x, p.hkv, num_groups);
+  kern<<<grid, tc::kThreads, L::kDynSmem, s>>>(p, unused);
+  return check_launch("attn_tc_kernel<cascade prefix>");
+}
+
+}  // namespace
+
+ra_status launch_cascade_prefix(const DecodeParams& d, const CascadeArgs& ca, int32_t head_dim,
+                                cudaStream_t stream) {
+  if (128 % d.group != 0)
+    return fail(RA_ERR_UNSUPPORTED, "GQA group %d does not divide the 128-row tile", d.group);
+  TcParams p{};
+  p.k_pool = d.k_pool;
+  p.v_pool = d.v_pool;
+  p.num_slots = d.num_slots;
+  p.hkv = d.hkv;
+  p.q = d.q;
+  p.hq = d.hq;
+  p.group = d.group;
+  p.scale_log2 = d.scale_log2;
+  p.table = d.table;
+  p.table_stride = d.table_stride;
+  p.table_rows = d.table_rows;
+  p.err = d.err;
+  p.rpi = d.rpi;
+  p.group_indptr = ca.group_indptr;
+  p.group_reqs = ca.group_reqs;
+  p.group_prefix_len = ca.group_prefix_len;
+  p.batch = d.batch;
+  p.max_seq_len = d.max_seq_len;
+  p.cchunk = d.cchunk;
+  p.max_csplits = d.max_csplits;
+  p.casc_o = d.casc_o;
+  p.casc_lse = d.casc_lse;
+  const int rows_per_tile = 128 / d.group;
+  const int mtiles = (ca.max_group_size + rows_per_tile - 1) / rows_per_tile;
+  const int grid_x = mtiles * d.max_csplits;
+  return head_dim == 128 ? launch_prefix<128>(p, grid_x, ca.num_groups, stream)
+                         : launch_prefix<64>(p, grid_x, ca.num_groups, stream);
+}
+
 }  // namespace ra
 
-extern "C" ra_status ra_extend_attention(const void*, const void*, int64_t, int32_t, int32_t, const void*, void*,
-                                         int32_t, float, const int32_t*, int64_t, int64_t, const int32_t*,
-                                         const int32_t*, const int32_t*, const int32_t*, int32_t, int64_t, int32_t,
-                                         int32_t, uint32_t*, ra_stream_t) {
-  ra::clear_error();
-  return ra::fail(RA_ERR_UNSUPPORTED, "extend not built yet");
+extern "C" ra_status ra_extend_attention(const void* k_pool, const void* v_pool, int64_t num_slots,
+                                         int32_t num_kv_heads, int32_t head_dim, const void* q, void* o,
+                                         int32_t num_q_heads, float sm_scale, const int32_t* req_to_token,
+                                         int64_t table_stride, int64_t table_rows, const int32_t* req_pool_indices,
+                                         const int32_t* prefix_lens, const int32_t* extend_lens,
+                                         const int32_t* qo_indptr, int32_t batch, int64_t total_q,
+                                         int32_t max_extend_len, int32_t max_prefix_len, uint32_t* device_error,
+                                         ra_stream_t stream) {
+  using namespace ra;
+  clear_error();
+  RA_REQUIRE(batch >= 0 && batch <= 65535, "batch must be in [0, 65535] (got %d)", batch);
+  RA_REQUIRE(total_q >= 0 && total_q < (int64_t(1) << 31), "total_q out of range");
+  RA_REQUIRE(num_kv_heads > 0 && num_q_heads > 0, "head counts must be > 0");
+  RA_REQUIRE(num_q_heads % num_kv_heads == 0, "num_q_heads (%d) must be a multiple of num_kv_heads (%d)",
+             num_q_heads, num_kv_heads);
+  RA_REQUIRE(num_slots > 0, "num_slots must be > 0");
+  RA_REQUIRE(std::isfinite(sm_scale) && sm_scale > 0.f, "sm_scale must be finite and > 0");
+  if (head_dim != 64 && head_dim != 128) return fail(RA_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+  const int32_t group = num_q_heads / num_kv_heads;
+  if (128 % group != 0) return fail(RA_ERR_UNSUPPORTED, "GQA group %d must divide 128", group);
+  if (batch == 0 || total_q == 0) return RA_OK;
+  RA_REQUIRE(max_extend_len >= 1 && max_prefix_len >= 0, "max_extend_len must be >= 1, max_prefix_len >= 0");
+  // each request needs prefix_lens[b] + extend_lens[b] <= table_stride (checked per request on the device)
+  RA_REQUIRE(table_stride >= max_extend_len && table_stride > max_prefix_len,
+             "table_stride (%lld) narrower than max_extend_len or max_prefix_len + 1", (long long)table_stride);
+  RA_REQUIRE(table_rows > 0, "table_rows must be > 0");
+  RA_REQUIRE(k_pool && v_pool && q && o && req_to_token && req_pool_indices && prefix_lens && extend_lens &&
+                 qo_indptr,
+             "null pointer argument");
+  RA_REQUIRE(aligned16(k_pool) && aligned16(v_pool) && aligned16(q) && aligned16(o),
+             "pools, q and o must be 16-byte aligned");
+  RA_REQUIRE(aligned4(req_to_token) && aligned4(req_pool_indices) && aligned4(prefix_lens) &&
+                 aligned4(extend_lens) && aligned4(qo_indptr),
+             "index arrays must be 4-byte aligned");
+
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  // q viewed as [total_q][Hq][D]; one box = 128/G tokens x the G heads of a kv head x 64 dims
+  const int rows_per_tile = 128 / group;
+  CUtensorMap qmap;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_q_heads),
+                        static_cast<cuuint64_t>(total_q)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                           static_cast<cuuint64_t>(num_q_heads) * head_dim * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(rows_per_tile)};
+  cuuint32_t elem[3] = {1, 1, 1};
+  CUresult cr = encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, elem,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled(q) failed (%d)", static_cast<int>(cr));
+
+  TcParams p{};
+  p.k_pool = static_cast<const __nv_bfloat16*>(k_pool);
+  p.v_pool = static_cast<const __nv_bfloat16*>(v_pool);
+  p.num_slots = num_slots;
+  p.hkv = num_kv_heads;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.hq = num_q_heads;
+  p.group = group;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.table = req_to_token;
+  p.table_stride = table_stride;
+  p.table_rows = table_rows;
+  p.err = device_error;
+  p.rpi = req_pool_indices;
+  p.prefix_lens = prefix_lens;
+  p.extend_lens = extend_lens;
+  p.qo_indptr = qo_indptr;
+  p.max_extend_len = max_extend_len;
+  p.max_prefix_len = max_prefix_len;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  const int max_tiles = (max_extend_len + rows_per_tile - 1) / rows_per_tile;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return head_dim == 128 ? launch_extend<128>(p, qmap, max_tiles, batch, s)
+                         : launch_extend<64>(p, qmap, max_tiles, batch, s);
 }

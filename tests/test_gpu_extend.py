@@ -1,0 +1,161 @@
+"""GPU parity: extend attention (tcgen05) and the cascade (prefix-grouped) decode
+against the CPU oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import prefix_shared_kv_ra_gb300 as ra
+import workloads as W
+from helpers import DeviceBatch, assert_close, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def check_extend(db: DeviceBatch, sel=None):
+    b = db.b
+    db.extend()
+    torch.cuda.synchronize()
+    assert int(db.err.item()) == 0, int(db.err.item())
+    got = to_f64(db.ext_o).reshape(-1, b.head_dim)
+    ref = oracle.extend_batch(b, sel=sel)
+    if sel is not None:
+        got = got[sel]
+    assert_close(got, ref, f"{b.name} extend")
+
+
+def test_extend_tiny_config():
+    e, _ = W.cfg1_tiny()
+    db = DeviceBatch(e)
+    db.store()
+    check_extend(db)
+
+
+@pytest.mark.parametrize("seed,hq,hkv,d,max_len", [
+    (0, 8, 2, 64, 40), (1, 32, 8, 128, 300), (2, 16, 2, 128, 700), (3, 8, 8, 128, 200),
+    (4, 64, 8, 128, 500), (5, 4, 2, 64, 900), (6, 16, 1, 128, 150), (7, 32, 2, 64, 260)])
+def test_extend_ragged(seed, hq, hkv, d, max_len):
+    b = W.random_mixed(seed, n_extend=6, n_decode=0, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                       max_len=max_len)
+    db = DeviceBatch(b)
+    db.store()
+    check_extend(db)
+
+
+def test_extend_prefix_zero_and_single_token_suffix():
+    b = W.random_mixed(11, n_extend=5, n_decode=0, num_q_heads=32, num_kv_heads=8, head_dim=128, max_len=300,
+                       share_prob=0.0, ext_lens=[1, 300, 1, 129, 128])
+    assert (b.ext_prefix_lens == 0).any() and (b.ext_extend_lens == 1).any()
+    db = DeviceBatch(b)
+    db.store()
+    check_extend(db)
+
+
+def test_extend_fewshot_full():
+    b = W.cfg3_fewshot_extend()
+    db = DeviceBatch(b)
+    db.store()
+    rng = np.random.default_rng(3)
+    n = b.total_q_extend * b.num_q_heads
+    sel = np.unique(np.concatenate([rng.choice(n, 4096, replace=False), np.arange(64), n - 64 + np.arange(64)]))
+    check_extend(db, sel=sel)
+
+
+def test_extend_multiturn_mix_sampled():
+    b = W.cfg5_multiturn_mix_70b()
+    db = DeviceBatch(b)
+    db.store()
+    rng = np.random.default_rng(4)
+    n = b.total_q_extend * b.num_q_heads
+    sel = np.sort(rng.choice(n, 1024, replace=False))
+    check_extend(db, sel=sel)
+
+
+def test_extend_matches_decode_for_the_last_token():
+    """The last suffix row of an extend equals a decode of that token (same context)."""
+    b = W.random_mixed(12, n_extend=4, n_decode=0, num_q_heads=32, num_kv_heads=8, head_dim=128, max_len=600)
+    db = DeviceBatch(b)
+    db.store()
+    db.extend()
+    last = b.ext_qo_indptr[1:] - 1
+    q = db.ext_q[torch.from_numpy(last.astype(np.int64)).to(db.dev)].contiguous()
+    o = torch.empty_like(q)
+    lens = torch.from_numpy((b.ext_prefix_lens + b.ext_extend_lens).astype(np.int32)).to(db.dev)
+    ws = torch.empty(ra.ra_decode_workspace_bytes(4, 32, 8, 128, int(lens.max())), dtype=torch.uint8,
+                     device=db.dev)
+    ra.ra_decode_attention(db.k_pool, db.v_pool, q, o, db.table, db.ext_rpi, lens, max_seq_len=int(lens.max()),
+                           sm_scale=b.sm_scale, workspace=ws)
+    torch.cuda.synchronize()
+    a = to_f64(db.ext_o[torch.from_numpy(last.astype(np.int64)).to(db.dev)])
+    assert_close(to_f64(o), a, "decode vs last extend row")
+
+
+def test_extend_bad_slot_flagged():
+    b = W.random_mixed(13, n_extend=2, n_decode=0, num_q_heads=8, num_kv_heads=2, head_dim=64, max_len=100)
+    db = DeviceBatch(b)
+    db.store()
+    db.table[b.ext_rpi[0], 0] = b.num_slots  # out of range
+    db.extend()
+    torch.cuda.synchronize()
+    assert int(db.err.item()) & ra.DEVERR_SLOT
+
+
+# ---------------------------------------------------------------- cascade decode
+def check_cascade(db: DeviceBatch, sel=None):
+    b = db.b
+    assert b.has_cascade()
+    db.decode(cascade=False)
+    torch.cuda.synchronize()
+    plain = to_f64(db.dec_o)
+    db.dec_o.zero_()
+    db.decode(cascade=True)
+    torch.cuda.synchronize()
+    assert int(db.err.item()) == 0, int(db.err.item())
+    casc = to_f64(db.dec_o)
+    got = casc.reshape(-1, b.head_dim)
+    ref = oracle.decode_batch(b, sel=sel)
+    if sel is not None:
+        got = got[sel]
+    assert_close(got, ref, f"{b.name} cascade decode")
+    assert_close(casc, plain, f"{b.name} cascade vs plain")
+
+
+def test_cascade_tiny_config():
+    _, d = W.cfg1_tiny()
+    db = DeviceBatch(d)
+    db.store()
+    check_cascade(db)
+
+
+@pytest.mark.parametrize("seed,hq,hkv,d,max_len", [
+    (20, 32, 8, 128, 900), (21, 64, 8, 128, 400), (22, 8, 2, 64, 300), (23, 16, 8, 128, 1300)])
+def test_cascade_ragged(seed, hq, hkv, d, max_len):
+    b = W.random_mixed(seed, n_extend=0, n_decode=24, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                       max_len=max_len, share_prob=0.9, with_cascade=True)
+    if not b.has_cascade():
+        pytest.skip("seed produced no group")
+    db = DeviceBatch(b)
+    db.store()
+    check_cascade(db)
+
+
+@pytest.mark.parametrize("name", ["cfg2_decode_8b", "cfg4_forked_decode_70b"])
+def test_cascade_full_workloads(name):
+    b = W.CONFIGS[name]()
+    db = DeviceBatch(b)
+    db.store()
+    check_cascade(db)
+
+
+def test_cascade_member_without_private_keys():
+    """A member whose whole context is the group prefix (P_g == L) only has prefix partials."""
+    b = W.random_mixed(24, n_extend=0, n_decode=6, num_q_heads=32, num_kv_heads=8, head_dim=128, max_len=500,
+                       share_prob=0.9, with_cascade=True)
+    if not b.has_cascade():
+        pytest.skip("seed produced no group")
+    g0 = b.casc_group_reqs[b.casc_group_indptr[0]:b.casc_group_indptr[1]]
+    # shrink the prefix to the shortest member's full length
+    b.casc_group_prefix_len[0] = min(b.casc_group_prefix_len[0], int(b.dec_seq_lens[g0].min()))
+    db = DeviceBatch(b)
+    db.store()
+    check_cascade(db)
