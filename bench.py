@@ -1,0 +1,485 @@
+#!/usr/bin/env python3
+"""Benchmark of the RadixAttention hot path on GB300 (one JSON line on stdout).
+
+One step = one pass of the whole path over one batch of the multi-turn chat
+workload (70B attention heads: 64 q / 8 kv, head_dim 128; 256 requests with
+lognormal contexts sharing prefixes through a radix tree at a ~70% token
+hit ratio; 32 extend requests + 224 decode requests; 2M-slot pool):
+  ra_kv_store (this step's 9.4K new tokens)  ->  ra_extend_attention  ->
+  ra_decode_attention.
+value = attention tokens (extend suffix tokens + decode tokens) per second
+with inputs resident in HBM; L2 is flushed (256 MB write) between steps.
+Extra objects: per-kernel roofline (decode KV GB/s vs measured HBM copy
+bandwidth, extend TFLOP/s vs measured dense BF16), e2e through the public API
+with host buffers, the CPU oracle as baseline, SM clocks during the timed
+region, and the same kernels on the decode (Llama-3-8B shape, system-prompt
+groups), few-shot extend and forked-decode workloads.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--no-extra]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn tokens/s; decode KV GB/s and extend TFLOP/s as % of GB300 roofline"
+UNIT = "tokens/s"
+WORKLOAD = ("multi-turn chat mix, 70B heads (64 q / 8 kv, head_dim 128, bf16): 256 requests, lognormal "
+            "contexts (median 2048, clipped 16..32768), radix-tree prefix sharing at 70% token hit ratio; "
+            "32 extend (suffix 64..512) + 224 decode; pool 2M slots")
+L2_FLUSH_BYTES = 256 << 20
+KV_BYTES_PER_TOKEN_HEAD = 2 * 128 * 2  # K + V row of one kv head, bf16
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+def extend_flops(b) -> float:
+    e = b.ext_extend_lens.astype(np.float64)
+    p = b.ext_prefix_lens.astype(np.float64)
+    return float(np.sum(b.num_q_heads * (e * p + e * (e + 1) / 2) * 4 * b.head_dim))
+
+
+def decode_bytes(b, cascade: bool = False) -> dict:
+    """Algorithmic decode bytes: every distinct K/V row the batch's contexts reference
+    (a row shared by several requests counts once), plus q, o and table entries.
+    `logical` counts every request's rows separately."""
+    rows = [b.req_to_token[r, :L] for r, L in zip(b.dec_rpi, b.dec_seq_lens)]
+    uniq = np.unique(np.concatenate(rows)).size if rows else 0
+    logical = int(np.sum(b.dec_seq_lens))
+    kv_row = b.num_kv_heads * b.head_dim * 2 * 2
+    qo = 2 * b.n_decode * b.num_q_heads * b.head_dim * 2
+    idx = logical * 4
+    return {"unique_tokens": int(uniq), "logical_tokens": logical,
+            "algorithmic": uniq * kv_row + qo + idx, "logical": logical * kv_row + qo + idx}
+
+
+def store_bytes(b) -> int:
+    return 2 * 2 * b.num_new_tokens * b.num_kv_heads * b.head_dim * 2  # read + write, K and V
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ["uuid", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, uuid: str):
+        self.uuid = uuid
+        self.proc = None
+        self.out = os.path.join("/tmp", f"ra_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.out, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS),
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.out):
+            return None
+        by_gpu = {}
+        for line in open(self.out):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                by_gpu.setdefault(parts[0], []).append((float(parts[1]), float(parts[2]), parts[5:]))
+            except ValueError:
+                continue
+        if not by_gpu:
+            return None
+        # this process's GPU by UUID; with one visible GPU its rows are the only ones
+        rows = by_gpu.get(self.uuid) or next(iter(by_gpu.values()))
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, _, flags in rows for n, v in zip(names, flags) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+class Step:
+    """The hot path on one batch, resident on the device."""
+
+    def __init__(self, b, dev, cascade: bool = False):
+        import torch
+        import prefix_shared_kv_ra_gb300 as ra
+        self.torch, self.ra, self.b, self.dev = torch, ra, b, dev
+        self.cascade = cascade and b.has_cascade()
+
+        def bf16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        def i32(a):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+        S, hkv, d = b.num_slots, b.num_kv_heads, b.head_dim
+        self.k_pool = torch.zeros((S, hkv, d), dtype=torch.bfloat16, device=dev)
+        self.v_pool = torch.zeros((S, hkv, d), dtype=torch.bfloat16, device=dev)
+        idx = torch.from_numpy(b.pool_slots.astype(np.int64)).to(dev)
+        self.k_pool.index_copy_(0, idx, bf16(b.pool_k))
+        self.v_pool.index_copy_(0, idx, bf16(b.pool_v))
+        self.host = {  # per-step inputs (pinned host copies for the e2e measurement)
+            "k_new": b.k_new, "v_new": b.v_new, "loc": b.out_cache_loc.astype(np.int32),
+            "ext_q": b.ext_q, "ext_rpi": b.ext_rpi, "ext_prefix": b.ext_prefix_lens, "ext_len": b.ext_extend_lens,
+            "ext_qo": b.ext_qo_indptr, "dec_q": b.dec_q, "dec_rpi": b.dec_rpi, "dec_lens": b.dec_seq_lens}
+        self.d = {k: (bf16(v) if v.dtype == np.uint16 else i32(v)) for k, v in self.host.items()}
+        self.table = i32(b.req_to_token)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ext_o = torch.empty_like(self.d["ext_q"])
+        self.dec_o = torch.empty_like(self.d["dec_q"])
+        self.casc = {}
+        if self.cascade:
+            self.casc = dict(group_indptr=i32(b.casc_group_indptr), group_reqs=i32(b.casc_group_reqs),
+                             group_prefix_len=i32(b.casc_group_prefix_len),
+                             max_group_prefix_len=int(b.casc_group_prefix_len.max()),
+                             max_group_size=int(np.diff(b.casc_group_indptr).max()))
+        ng = b.casc_group_indptr.size - 1 if self.cascade else 0
+        nws = ra.ra_decode_workspace_bytes(max(b.n_decode, 1), b.num_q_heads, hkv, d, max(b.max_seq_len, 1), ng,
+                                           self.casc.get("max_group_prefix_len", 0),
+                                           self.casc.get("max_group_size", 0))
+        self.ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
+        # kernel launches per step (the library's launch structure)
+        self.launches = 1 + (1 if b.n_extend else 0) + ((2 + (2 if self.cascade else 0)) if b.n_decode else 0)
+
+    def run(self, d=None, events=None):
+        ra, b = self.ra, self.b
+        d = d or self.d
+        ev = events or [None] * 4
+        if ev[0] is not None:
+            ev[0].record()
+        ra.ra_kv_store(self.k_pool, self.v_pool, d["k_new"], d["v_new"], d["loc"], device_error=self.err)
+        if ev[1] is not None:
+            ev[1].record()
+        if b.n_extend:
+            ra.ra_extend_attention(self.k_pool, self.v_pool, d["ext_q"], self.ext_o, self.table, d["ext_rpi"],
+                                   d["ext_prefix"], d["ext_len"], d["ext_qo"], max_extend_len=b.max_extend_len,
+                                   max_prefix_len=b.max_prefix_len, sm_scale=b.sm_scale, device_error=self.err)
+        if ev[2] is not None:
+            ev[2].record()
+        if b.n_decode:
+            ra.ra_decode_attention(self.k_pool, self.v_pool, d["dec_q"], self.dec_o, self.table, d["dec_rpi"],
+                                   d["dec_lens"], max_seq_len=b.max_seq_len, sm_scale=b.sm_scale,
+                                   workspace=self.ws, device_error=self.err, **self.casc)
+        if ev[3] is not None:
+            ev[3].record()
+
+
+def time_steps(step, steps: int, warmup: int, flush, sample_clocks_uuid=None):
+    torch = step.torch
+    for _ in range(warmup):
+        flush.zero_()
+        step.run()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    sampler = ClockSampler(sample_clocks_uuid) if sample_clocks_uuid is not None else None
+    if sampler:
+        sampler.__enter__()
+    try:
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for k in range(steps):
+            flush.zero_()
+            step.run(events=evs[k])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    finally:
+        if sampler:
+            sampler.__exit__(None, None, None)
+    per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evs])  # ms: store, extend, decode
+    total = np.array([e[0].elapsed_time(e[3]) for e in evs])
+    err = int(step.err.item())
+    return {"store_ms": per[:, 0], "extend_ms": per[:, 1], "decode_ms": per[:, 2], "step_ms": total,
+            "wall_s": wall, "clocks": sampler.summary() if sampler else None, "device_error": err}
+
+
+def e2e_steps(step, steps: int, warmup: int, flush):
+    """Same step through the public API with host buffers: H2D of the step's inputs from
+    pinned memory, the three calls, D2H of both outputs, all inside the timed region."""
+    torch = step.torch
+    pinned = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16) if v.dtype == np.uint16
+                                  else np.ascontiguousarray(v, dtype=np.int32)).pin_memory()
+              for k, v in step.host.items()}
+    dev_bufs = {k: torch.empty(v.shape, dtype=v.dtype, device=step.dev) for k, v in pinned.items()}
+    out_ext = torch.empty(step.ext_o.shape, dtype=torch.int16).pin_memory()
+    out_dec = torch.empty(step.dec_o.shape, dtype=torch.int16).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = out_ext.numel() * 2 + out_dec.numel() * 2
+
+    def one(ev=None):
+        if ev:
+            ev[0].record()
+        for k, v in pinned.items():
+            dev_bufs[k].copy_(v, non_blocking=True)
+        d = {k: (v.view(torch.bfloat16) if v.dtype == torch.int16 else v) for k, v in dev_bufs.items()}
+        step.run(d=d)
+        out_ext.copy_(step.ext_o.view(torch.int16), non_blocking=True)
+        out_dec.copy_(step.dec_o.view(torch.int16), non_blocking=True)
+        if ev:
+            ev[1].record()
+
+    for _ in range(warmup):
+        flush.zero_()
+        one()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for k in range(steps):
+        flush.zero_()
+        one(evs[k])
+    torch.cuda.synchronize()
+    ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    return ms, h2d, d2h
+
+
+def extra_kernels(dev, flush, peaks, reps: int = 20):
+    """The same kernels on the other workloads (parity-tested elsewhere): per-kernel roofline."""
+    import workloads as W
+    out = {}
+    specs = [("decode_8b_system_prompts", W.cfg2_decode_8b, (False, True)),
+             ("extend_fewshot_3000", W.cfg3_fewshot_extend, (False,)),
+             ("decode_70b_forked_8192", W.cfg4_forked_decode_70b, (False, True))]
+    for name, fn, modes in specs:
+        b = fn()
+        for casc in modes:
+            st = Step(b, dev, cascade=casc)
+            st.run()  # store once: the pool then holds this step's tokens
+            r = time_steps(st, reps, 3, flush)
+            key = name + ("_cascade" if casc else "")
+            if b.n_extend:
+                ms = float(np.median(r["extend_ms"]))
+                fl = extend_flops(b)
+                out[key] = {"kernel": "extend (tcgen05)", "ms": ms, "tokens_per_s": b.total_q_extend / ms * 1e3,
+                            "tflops": fl / ms / 1e9, "frac_of_measured_bf16": fl / ms / 1e9 / peaks["bf16_tflops"]}
+            else:
+                ms = float(np.median(r["decode_ms"]))
+                db = decode_bytes(b)
+                gbs = db["algorithmic"] / ms / 1e6
+                out[key] = {"kernel": "decode" + (" + cascade prefix pass" if casc else ""), "ms": ms,
+                            "tokens_per_s": b.n_decode / ms * 1e3, "algorithmic_bytes": db["algorithmic"],
+                            "gbs": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
+                            "effective_gbs": db["logical"] / ms / 1e6}
+            out[key]["device_error"] = r["device_error"]
+            del st
+    return out
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+def oracle_sample(b, budget_s: float, seed: int = 0):
+    """Time the fp64 oracle on a random sample of the step's query rows, about `budget_s`
+    seconds of work, and extrapolate to the whole step by key visits."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    pool = oracle.pool_after_store(b)
+    hq = b.num_q_heads
+    # key visits per query row
+    ext_keys = np.repeat(np.concatenate([b.ext_prefix_lens[i] + 1 + np.arange(b.ext_extend_lens[i])
+                                         for i in range(b.n_extend)]) if b.n_extend else np.zeros(0), hq)
+    dec_keys = np.repeat(b.dec_seq_lens.astype(np.float64), hq)
+    total_visits = float(ext_keys.sum() + dec_keys.sum())
+    threads = oracle.num_threads()
+
+    def timed(n_e, n_d):
+        se = np.sort(rng.choice(ext_keys.size, size=min(n_e, ext_keys.size), replace=False)) if ext_keys.size else None
+        sd = np.sort(rng.choice(dec_keys.size, size=min(n_d, dec_keys.size), replace=False)) if dec_keys.size else None
+        t0 = time.perf_counter()
+        if se is not None:
+            oracle.extend_batch(b, sel=se, pool=pool)
+        if sd is not None:
+            oracle.decode_batch(b, sel=sd, pool=pool)
+        v = (ext_keys[se].sum() if se is not None else 0) + (dec_keys[sd].sum() if sd is not None else 0)
+        return time.perf_counter() - t0, float(v)
+
+    # calibrate on a small sample, then time one sample sized to about budget_s
+    dt, v = timed(64, 64)
+    scale = max(1.0, budget_s / max(dt, 1e-3))
+    n_e = int(min(ext_keys.size, 64 * scale))
+    n_d = int(min(dec_keys.size, 64 * scale))
+    spent, visits = timed(n_e, n_d)
+    est_step_s = spent * total_visits / max(visits, 1.0)
+    tokens = b.total_q_extend + b.n_decode
+    return {"value": tokens / est_step_s, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{int(visits)} of {int(total_visits)} key visits ({100 * visits / total_visits:.2f}%) of "
+                      f"random query rows, {spent:.1f} s, extrapolated by key visits", "seconds": spent}
+
+
+def run_reference(args):
+    import workloads as W
+    b = W.cfg5_multiturn_mix_70b()
+    res = [oracle_sample(b, args.ref_budget, seed=k) for k in range(args.warmup + args.steps)]
+    timed = res[args.warmup:]
+    val = float(np.mean([r["value"] for r in timed]))
+    tokens = b.total_q_extend + b.n_decode
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tokens / val * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": 256, "tokens_per_step": tokens,
+                       "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": timed[0]["cores"], "kind": "oracle",
+                             "sample": timed[0]["sample"]},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the per-kernel runs on the other workloads")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds of oracle work per reference step")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args)
+        return
+
+    import torch
+    import prefix_shared_kv_ra_gb300 as ra
+    from prefix_shared_kv_ra_gb300 import _build
+    import workloads as W
+
+    if not os.path.exists(_build.LIB):
+        _build.build()
+    ra.load()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks = load_peaks()
+
+    # independent replicas: each rank draws its own batch of the same workload
+    b = W.cfg5_multiturn_mix_70b(seed=5 + rank)
+    step = Step(b, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = ""
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    r = time_steps(step, args.steps, args.warmup, flush, sample_clocks_uuid=uuid)
+    step_ms = float(np.mean(r["step_ms"]))
+    if dist:
+        t = torch.tensor([step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+        dist.barrier()
+    tokens = b.total_q_extend + b.n_decode
+    value = tokens * world / step_ms * 1e3
+
+    e2e_ms, h2d, d2h = e2e_steps(step, args.steps, args.warmup, flush)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if rank != 0:
+        dist.barrier()
+        dist.destroy_process_group()
+        return
+
+    ext_ms = float(np.mean(r["extend_ms"]))
+    dec_ms = float(np.mean(r["decode_ms"]))
+    st_ms = float(np.mean(r["store_ms"]))
+    fl = extend_flops(b)
+    dbytes = decode_bytes(b)
+    ext_tf = fl / ext_ms / 1e9
+    dec_gbs = dbytes["algorithmic"] / dec_ms / 1e6
+    # dominant kernel of the step: the one with the larger share of the step time
+    if ext_ms >= dec_ms:
+        roof = {"kernel": "attn_tc_kernel<extend>", "bound": "tensor", "achieved": ext_tf,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ext_tf / peaks["bf16_tflops"],
+                "traffic": None, "peak_source": peaks["source"] + " bf16 burst",
+                "per_launch": {"flops": fl, "ms": ext_ms}}
+    else:
+        roof = {"kernel": "decode_split_kernel + decode_combine_kernel", "bound": "hbm", "achieved": dec_gbs,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
+                "traffic": None, "peak_source": peaks["source"] + " HBM copy",
+                "per_launch": {"bytes": dbytes["algorithmic"], "ms": dec_ms}}
+    extra = {} if args.no_extra else extra_kernels(dev, flush, peaks)
+    cpu = oracle_sample(b, args.cpu_budget)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": 256 * world, "tokens_per_step": tokens * world,
+                   "extend_tokens": b.total_q_extend, "decode_tokens": b.n_decode, "l2": "flushed (256 MB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "hit_ratio": round(b.meta["construction_hit_ratio"], 4)},
+        "roofline": roof,
+        "kernels": {
+            "step_breakdown_ms": {"kv_store": st_ms, "extend": ext_ms, "decode": dec_ms},
+            "extend": {"tflops": ext_tf, "frac_of_measured_bf16": ext_tf / peaks["bf16_tflops"],
+                       "flops": fl},
+            "decode": {"gbs": dec_gbs, "frac_of_measured_hbm": dec_gbs / peaks["hbm_gbs"],
+                       "effective_gbs": dbytes["logical"] / dec_ms / 1e6, "unique_tokens": dbytes["unique_tokens"],
+                       "logical_tokens": dbytes["logical_tokens"]},
+            "kv_store": {"gbs": store_bytes(b) / st_ms / 1e6},
+            "other_workloads": extra,
+        },
+        "cpu_baseline": {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "e2e": {"value": tokens * world / e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": step.launches * args.steps,
+        "clocks": r["clocks"],
+        "device_error": r["device_error"],
+        "peaks": peaks,
+    }
+    print(json.dumps(line))
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
