@@ -157,6 +157,33 @@ size_t ra_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num
                                  int32_t max_seq_len, int32_t num_groups, int32_t max_group_prefix_len,
                                  int32_t max_group_size);
 
+/*
+ * ra_decode_attention_static -- ra_decode_attention for callers that cannot
+ * allocate device memory.  The paper has no counterpart: this is an interface
+ * addition for callers such as a plugin that runs under a host framework's
+ * fixed memory plan and may not call cudaMalloc, or a runtime that has no
+ * device allocator of its own.
+ *   Same arguments and results as ra_decode_attention, without the workspace:
+ *   the split-KV scratch lives in one file-scope device array of
+ *   RA_DECODE_STATIC_SCRATCH_BYTES that every GPU loading this library holds
+ *   until the process exits.  Nothing is allocated or freed by the call.
+ *   A call whose ra_decode_workspace_bytes(...) exceeds that size returns
+ *   RA_ERR_WORKSPACE with a message and launches nothing.
+ *   The first call on a device (with that device current) looks up the array's
+ *   device address; make that first call outside any stream capture.
+ *   All calls share the array and it keeps the last call's contents: calls
+ *   that overlap on the GPU (other streams, unordered threads) race on it.
+ */
+#define RA_DECODE_STATIC_SCRATCH_BYTES (32u << 20)
+ra_status ra_decode_attention_static(const void* k_pool, const void* v_pool, int64_t num_slots,
+                                     int32_t num_kv_heads, int32_t head_dim, const void* q, void* o,
+                                     int32_t num_q_heads, float sm_scale, const int32_t* req_to_token,
+                                     int64_t table_stride, int64_t table_rows, const int32_t* req_pool_indices,
+                                     const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+                                     int32_t num_groups, const int32_t* group_indptr, const int32_t* group_reqs,
+                                     const int32_t* group_prefix_len, int32_t max_group_prefix_len,
+                                     int32_t max_group_size, uint32_t* device_error, ra_stream_t stream);
+
 /* Static description of a status code. */
 const char* ra_status_string(ra_status status);
 

@@ -23,10 +23,12 @@ import torch
 from . import _build
 
 __all__ = ["RAError", "ra_kv_store", "ra_extend_attention", "ra_decode_attention", "ra_decode_workspace_bytes",
+           "ra_decode_attention_static", "RA_DECODE_STATIC_SCRATCH_BYTES",
            "ra_abi_version", "library_path", "load", "DEVERR_SLOT", "DEVERR_TABLE", "DEVERR_LENGTH",
            "DEVERR_TIMEOUT"]
 
 RA_OK = 0
+RA_DECODE_STATIC_SCRATCH_BYTES = 32 << 20  # size of the library's static decode scratch (include/ra.h)
 DEVERR_SLOT, DEVERR_TABLE, DEVERR_LENGTH, DEVERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 _lib = None
 
@@ -57,6 +59,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                                         i32, i32, P, P]
     lib.ra_decode_attention.argtypes = [P, P, i64, i32, i32, P, P, i32, f32, P, i64, i64, P, P, i32, i32, i32,
                                         P, P, P, i32, i32, P, sz, P, P]
+    lib.ra_decode_attention_static.argtypes = [P, P, i64, i32, i32, P, P, i32, f32, P, i64, i64, P, P, i32, i32,
+                                               i32, P, P, P, i32, i32, P, P]
+    lib.ra_decode_attention_static.restype = ctypes.c_int
     lib.ra_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
     lib.ra_decode_workspace_bytes.restype = sz
     for f in (lib.ra_kv_store, lib.ra_extend_attention, lib.ra_decode_attention, lib.ra_abi_version):
@@ -166,3 +171,29 @@ def ra_decode_attention(k_pool: torch.Tensor, v_pool: torch.Tensor, q: torch.Ten
         _ptr(group_prefix_len, i32, "group_prefix_len", dev), int(max_group_prefix_len), int(max_group_size),
         ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _ptr(device_error, i32, "device_error", dev),
         _stream(dev, stream)))
+
+
+def ra_decode_attention_static(k_pool: torch.Tensor, v_pool: torch.Tensor, q: torch.Tensor, o: torch.Tensor,
+                               req_to_token: torch.Tensor, req_pool_indices: torch.Tensor, seq_lens: torch.Tensor, *,
+                               max_seq_len: int, sm_scale: float, group_indptr: Optional[torch.Tensor] = None,
+                               group_reqs: Optional[torch.Tensor] = None,
+                               group_prefix_len: Optional[torch.Tensor] = None, max_group_prefix_len: int = 0,
+                               max_group_size: int = 0, device_error: Optional[torch.Tensor] = None,
+                               stream=None) -> None:
+    """ra_decode_attention without a workspace argument, for callers that cannot allocate:
+    the library's static device scratch (RA_DECODE_STATIC_SCRATCH_BYTES) is used instead."""
+    dev = k_pool.device
+    S, hkv, d = k_pool.shape
+    batch, hq, dq = q.shape
+    if dq != d or o.shape != q.shape:
+        raise ValueError("q/o shape mismatch")
+    bf, i32 = torch.bfloat16, torch.int32
+    ng = 0 if group_indptr is None else group_indptr.shape[0] - 1
+    _check(load().ra_decode_attention_static(
+        _ptr(k_pool, bf, "k_pool", dev), _ptr(v_pool, bf, "v_pool", dev), S, hkv, d, _ptr(q, bf, "q", dev),
+        _ptr(o, bf, "o", dev), hq, float(sm_scale), _ptr(req_to_token, i32, "req_to_token", dev),
+        req_to_token.shape[1], req_to_token.shape[0], _ptr(req_pool_indices, i32, "req_pool_indices", dev),
+        _ptr(seq_lens, i32, "seq_lens", dev), batch, int(max_seq_len), ng,
+        _ptr(group_indptr, i32, "group_indptr", dev), _ptr(group_reqs, i32, "group_reqs", dev),
+        _ptr(group_prefix_len, i32, "group_prefix_len", dev), int(max_group_prefix_len), int(max_group_size),
+        _ptr(device_error, i32, "device_error", dev), _stream(dev, stream)))

@@ -1,0 +1,80 @@
+// decode_static.cu -- ra_decode_attention_static: decode attention for callers
+// that cannot allocate device memory.
+//
+// ra_decode_attention needs a caller-provided workspace for its split-KV
+// partial results.  Some callers have no way to get one: a plugin that runs
+// inside a host framework's pre-planned memory budget and may not call
+// cudaMalloc after start-up, a runtime without a device allocator of its own,
+// or code that must not touch the allocator at all.  This entry point takes the
+// same inputs and outputs but keeps its scratch in one file-scope device array
+// of RA_DECODE_STATIC_SCRATCH_BYTES (32 MiB), which every GPU that loads this
+// library holds until the process exits.
+//
+// Set-up: the first call on a device, with that device current, looks up the
+// array's device address with cudaGetSymbolAddress (the array's name in host
+// code is only a host-side stand-in) and caches it per device.  Make that first
+// call outside any stream capture.  The call allocates nothing: no cudaMalloc,
+// no cudaFree, no allocating library routine.  It then runs the normal decode
+// path with the array as its workspace, so its results are those of
+// ra_decode_attention.  All calls share the one array and it keeps the last
+// call's contents (the decode path writes every partial before reading it and
+// clears the one field that must start at zero itself), so calls that overlap
+// on the GPU -- on different streams, or on one stream from several threads
+// without ordering -- race on it.
+#include <mutex>
+
+#include "api_common.h"
+
+namespace ra {
+namespace {
+
+__device__ __align__(256) uint8_t g_decode_scratch[RA_DECODE_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_decode_scratch on the current device (looked up once per device).
+ra_status scratch_for_current_device(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(RA_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return fail(RA_ERR_CUDA, "cudaGetSymbolAddress(static decode scratch): %s", cudaGetErrorString(e));
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return RA_OK;
+}
+
+}  // namespace
+}  // namespace ra
+
+extern "C" ra_status ra_decode_attention_static(
+    const void* k_pool, const void* v_pool, int64_t num_slots, int32_t num_kv_heads, int32_t head_dim, const void* q,
+    void* o, int32_t num_q_heads, float sm_scale, const int32_t* req_to_token, int64_t table_stride,
+    int64_t table_rows, const int32_t* req_pool_indices, const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+    int32_t num_groups, const int32_t* group_indptr, const int32_t* group_reqs, const int32_t* group_prefix_len,
+    int32_t max_group_prefix_len, int32_t max_group_size, uint32_t* device_error, ra_stream_t stream) {
+  using namespace ra;
+  clear_error();
+  void* scratch = nullptr;
+  if (ra_status st = scratch_for_current_device(&scratch)) return st;
+  const size_t need = ra_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                                                num_groups, max_group_prefix_len, max_group_size);
+  if (need > static_cast<size_t>(RA_DECODE_STATIC_SCRATCH_BYTES))
+    return fail(RA_ERR_WORKSPACE,
+                "this decode needs %zu bytes of scratch; the static scratch holds %zu "
+                "(use ra_decode_attention with a caller workspace)",
+                need, static_cast<size_t>(RA_DECODE_STATIC_SCRATCH_BYTES));
+  return ra_decode_attention(k_pool, v_pool, num_slots, num_kv_heads, head_dim, q, o, num_q_heads, sm_scale,
+                             req_to_token, table_stride, table_rows, req_pool_indices, seq_lens, batch, max_seq_len,
+                             num_groups, group_indptr, group_reqs, group_prefix_len, max_group_prefix_len,
+                             max_group_size, scratch, static_cast<size_t>(RA_DECODE_STATIC_SCRATCH_BYTES),
+                             device_error, stream);
+}
