@@ -357,6 +357,32 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+# ----------------------------------------------------------------------------- ncu cases
+PROFILE_CASES = {
+    "extend_fewshot": ("cfg3_fewshot_extend", False),
+    "decode_8b": ("cfg2_decode_8b", False),
+    "decode_8b_cascade": ("cfg2_decode_8b", True),
+    "decode_70b_forked_cascade": ("cfg4_forked_decode_70b", True),
+    "multiturn_mix": ("cfg5_multiturn_mix_70b", False),
+}
+
+
+def run_profile_case(name: str, steps: int):
+    """Run `steps` passes (store, extend, decode) of one workload, untimed, for a profiler."""
+    import torch
+    import prefix_shared_kv_ra_gb300 as ra
+    import workloads as W
+    ra.load()
+    cfg, cascade = PROFILE_CASES[name]
+    dev = torch.device("cuda:0")
+    st = Step(W.CONFIGS[cfg](), dev, cascade=cascade)
+    for _ in range(steps):
+        st.run()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": name, "steps": steps, "launches_per_step": st.launches,
+                      "device_error": int(st.err.item())}))
+
+
 # ----------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -367,8 +393,12 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the per-kernel runs on the other workloads")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds of oracle work per reference step")
+    ap.add_argument("--profile", default=None, choices=sorted(PROFILE_CASES),
+                    help="untimed: run the hot path of one workload --steps times (for an ncu capture)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.profile:
+        return run_profile_case(args.profile, args.steps)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -104,7 +104,8 @@ ra_status ra_kv_store(void* k_pool, void* v_pool, int64_t num_slots, int32_t num
  * Rows with extend_lens[b] == 0 write nothing; prefix_lens[b] == 0 is plain
  * causal attention.  batch == 0 or total_q == 0 is a no-op.
  * Runs on tcgen05 tensor cores with TMEM accumulators; K/V rows are gathered
- * from the pool by TMA.
+ * from the pool into 128B-swizzled shared-memory tiles, the query tile comes
+ * in by one TMA tile load.
  */
 ra_status ra_extend_attention(const void* k_pool, const void* v_pool, int64_t num_slots, int32_t num_kv_heads,
                               int32_t head_dim, const void* q, void* o, int32_t num_q_heads, float sm_scale,
