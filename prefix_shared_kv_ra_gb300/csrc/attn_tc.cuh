@@ -377,40 +377,45 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       }
       tc_wait_ld();
       const int32_t key0 = kbeg + j * kKeys;
-      float mx = -INFINITY;
+      // row max of the raw scores (scale > 0 commutes with max), 8 independent chains
+      float mx8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
       if (key0 + kKeys > lim) {
 #pragma unroll
         for (int c = 0; c < kKeys; ++c) {
-          const float x = (key0 + c < lim) ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
-          sr[c] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
+          if (key0 + c >= lim) sr[c] = __float_as_uint(-INFINITY);
+          mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sr[c]));
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) {
-          const float x = __uint_as_float(sr[c]) * p.scale_log2;
-          sr[c] = __float_as_uint(x);
-          mx = fmaxf(mx, x);
-        }
+        for (int c = 0; c < kKeys; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sr[c]));
       }
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.scale_log2;
       const float m_new = fmaxf(m_used, mx);
       const bool resc = m_new > m_used + kRescaleThreshold;
       const float m_ref = resc ? m_new : m_used;
       const float m_sub = (m_ref == -INFINITY) ? 0.f : m_ref;
       const float alpha = resc ? ex2(m_used - m_sub) : 1.f;
-      float rowsum = 0.f;
+      // p = 2^(s * scale_log2 - m_ref): one FMA + one MUFU per score; 8 independent partial sums
+      float sum8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
 #pragma unroll
       for (int c = 0; c < kKeys / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(__uint_as_float(sr[c * 32 + 2 * e]) - m_sub);
-          const float p1 = ex2(__uint_as_float(sr[c * 32 + 2 * e + 1]) - m_sub);
-          rowsum += p0 + p1;
+          const float p0 = ex2(fmaf(__uint_as_float(sr[c * 32 + 2 * e]), p.scale_log2, -m_sub));
+          const float p1 = ex2(fmaf(__uint_as_float(sr[c * 32 + 2 * e + 1]), p.scale_log2, -m_sub));
+          sum8[(2 * e) & 7] += p0;
+          sum8[(2 * e + 1) & 7] += p1;
           pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tmem + lane_addr + sb * kColS1 + c * 16, pk);
       }
+      const float rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       l = l * alpha + rowsum;
       if (j > 0) {
         // Observe PV_{j-1} before releasing P_j: bar_o then never runs two phases ahead of

@@ -37,248 +37,307 @@ namespace ra {
 
 namespace {
 
-constexpr int kSlab = 16;
+constexpr int kSlab = 16;          // keys per ring stage (the MMA M side)
+constexpr int kMaxChunk = 1024;    // keys per item (plan_decode never exceeds it)
+constexpr int kMaxStages = 8;
+constexpr int kItemRing = 16;      // > kMaxStages: an item id is never overwritten before it is read
+constexpr int kHdrBytes = 256 + 2 * kMaxChunk * 4;  // barriers, item ring, flags, 2 slot buffers
+constexpr int kSmemLimit = 227 * 1024;
 
-template <int D>
-struct DecodeShape {
-  static constexpr int kRowStride = D * 2 + 16;  // padded: 8 rows of a ldmatrix hit 8 distinct bank groups
-  static constexpr int kStageBytes = 2 * kSlab * kRowStride;
-  static constexpr int kKT = D / 16;
+// One work item: keys [k0, k1) of request b for the kv heads of head group hg.
+struct Item {
+  int32_t b, split, hg, k0, k1, start, n_splits, row;
 };
 
-template <int D, int NWARPS, int NSTAGE>
-constexpr int decode_smem_bytes() {
-  return 128 + NWARPS * NSTAGE * DecodeShape<D>::kStageBytes;
-}
-
-__device__ __forceinline__ int32_t load_slot(const int32_t* __restrict__ row_ptr, int32_t key,
-                                             int64_t num_slots, uint32_t* err) {
-  int32_t s = __ldg(row_ptr + key);
-  if (s < 0 || s >= num_slots) {
-    flag_error(err, RA_DEVERR_SLOT);
-    s = 0;
-  }
-  return s;
-}
-
-template <int D, int NWARPS, int NSTAGE>
-__global__ void __launch_bounds__(NWARPS * 32, 2) decode_split_kernel(const DecodeParams p) {
-  using Sh = DecodeShape<D>;
-  constexpr int RS = Sh::kRowStride;
-  constexpr int KT = Sh::kKT;
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ int s_abort;
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int split = blockIdx.x;
-  const int kh = blockIdx.y;
-  const int b = blockIdx.z;
-
-  // ---- per-request range (uniform over the CTA)
-  int32_t L = __ldg(p.seq_lens + b);
-  const int32_t row = __ldg(p.rpi + b);
-  if (row < 0 || row >= p.table_rows || L < 1) {
-    if (split == 0 && kh == 0 && threadIdx.x == 0)
-      flag_error(p.err, (row < 0 || row >= p.table_rows) ? RA_DEVERR_TABLE : RA_DEVERR_LENGTH);
-    return;
+// Item `idx` = (b * max_splits + split) * n_hgroups + hg: request-major, so the empty splits of a
+// request (split >= its split count) are one contiguous run the producer can skip at once, and
+// requests next to each other (often sharing a prefix) are in flight together. False if empty.
+__device__ __forceinline__ bool decode_item(const DecodeParams& p, int32_t idx, Item& it, bool report) {
+  it.hg = idx % p.n_hgroups;
+  const int32_t t = idx / p.n_hgroups;
+  it.split = t % p.max_splits;
+  it.b = t / p.max_splits;
+  int32_t L = __ldg(p.seq_lens + it.b);
+  it.row = __ldg(p.rpi + it.b);
+  const bool first = report && it.split == 0 && it.hg == 0;
+  if (it.row < 0 || it.row >= p.table_rows || L < 1) {
+    if (first) flag_error(p.err, (it.row < 0 || it.row >= p.table_rows) ? RA_DEVERR_TABLE : RA_DEVERR_LENGTH);
+    return false;
   }
   if (L > p.max_seq_len) {
-    if (split == 0 && kh == 0 && threadIdx.x == 0) flag_error(p.err, RA_DEVERR_LENGTH);
+    if (first) flag_error(p.err, RA_DEVERR_LENGTH);
     L = p.max_seq_len;
   }
-  int32_t start = p.key_start ? __ldg(p.key_start + b) : 0;
-  start = start < 0 ? 0 : (start > L ? L : start);
-  const int32_t n_keys_total = L - start;
-  const int32_t n_splits = (n_keys_total + p.chunk - 1) / p.chunk;
-  if (split >= n_splits) return;
-  const int32_t k0 = start + split * p.chunk;
-  const int32_t k1 = min(L, k0 + p.chunk);
-  const int32_t n_slabs = (k1 - k0 + kSlab - 1) / kSlab;
-  const int32_t my_slabs = warp < n_slabs ? (n_slabs - warp + NWARPS - 1) / NWARPS : 0;
-  const int32_t* __restrict__ row_ptr = p.table + static_cast<int64_t>(row) * p.table_stride;
+  int32_t start = p.key_start ? __ldg(p.key_start + it.b) : 0;
+  it.start = start < 0 ? 0 : (start > L ? L : start);
+  it.n_splits = (L - it.start + p.chunk - 1) / p.chunk;
+  if (it.split >= it.n_splits) return false;
+  it.k0 = it.start + it.split * p.chunk;
+  it.k1 = min(L, it.k0 + p.chunk);
+  return true;
+}
 
-  // ---- shared memory: [barriers (128 B)] [warp 0 stages] [warp 1 stages] ...
-  const uint32_t bar0 = smem_u32(smem) + warp * NSTAGE * 8;
-  const uint32_t data0 = smem_u32(smem) + 128 + warp * NSTAGE * Sh::kStageBytes;
-  if (threadIdx.x == 0) s_abort = 0;
-  if (lane == 0) {
-    for (int s = 0; s < NSTAGE; ++s) mbar_init(bar0 + s * 8, 1);
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Persistent split-KV decode.  One CTA per SM pulls (request, split, head group) items
+// from a counter.  Warp `hpc` is the producer: per 16-key slab it copies each key's K and
+// V rows of the whole head group (hpc * D * 2 contiguous bytes) with one cp.async.bulk
+// each into a ring stage; consumer warp w owns kv head hg * hpc + w of every item.
+template <int D>
+__global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + 1), 1) decode_kernel(const DecodeParams p) {
+  constexpr int KT = D / 16;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nc = p.hpc;
+  const int ns = p.nstage;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t full0 = sbase;        // ns mbarriers
+  const uint32_t empty0 = sbase + 64;  // ns mbarriers
+  volatile int32_t* s_items = reinterpret_cast<volatile int32_t*>(smem + 128);
+  volatile int32_t* s_abort = reinterpret_cast<volatile int32_t*>(smem + 192);
+  int32_t* s_slots = reinterpret_cast<int32_t*>(smem + 256);
+  const uint32_t stage0 = sbase + kHdrBytes;
+  const int RS = p.row_stride;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ns; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, nc);
+    }
+    *s_abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
+  const int row_bytes = p.hpc * D * 2;
 
-  // ---- Q^T fragments (B operand): column g = lane/4 is q head kh*G + g
-  const int g = lane >> 2;
-  const int tq = lane & 3;
-  uint32_t qf[KT][2];
-  {
-    const bool live = g < p.group;
-    const __nv_bfloat16* qrow = p.q + (static_cast<int64_t>(b) * p.hq + kh * p.group + (live ? g : 0)) * D;
-#pragma unroll
-    for (int kk = 0; kk < KT; ++kk) {
-      qf[kk][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * tq)) : 0u;
-      qf[kk][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * tq)) : 0u;
-    }
-  }
-
-  const __nv_bfloat16* kv_base = (lane < 16 ? p.k_pool : p.v_pool) + static_cast<int64_t>(kh) * D;
-  const int64_t slot_stride = static_cast<int64_t>(p.hkv) * D;
-  // key handled by this lane's copy in slab i (rows past the range repeat the last key: finite data, weight 0)
-  auto slab_key = [&](int32_t i) {
-    const int32_t key = k0 + (warp + i * NWARPS) * kSlab + (lane & 15);
-    return key < k1 ? key : k1 - 1;
-  };
-  auto issue = [&](int32_t i, int32_t slot) {
-    const int st = i % NSTAGE;
-    if (lane == 0) mbar_arrive_expect_tx(bar0 + st * 8, 2 * kSlab * D * 2);
+  if (warp == nc) {
+    // ================================================================ producer
+    auto claim = [&]() -> int32_t {
+      for (;;) {
+        int32_t idx = 0;
+        if (lane == 0) idx = atomicAdd(p.counter, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        if (idx >= p.n_items) return -1;
+        Item it;
+        if (decode_item(p, idx, it, lane == 0)) return idx;
+        // the rest of this request's items are empty too: move everyone past them
+        const int32_t per_req = p.max_splits * p.n_hgroups;
+        if (lane == 0) atomicMax(p.counter, (idx / per_req + 1) * per_req);
+      }
+    };
+    auto prefetch = [&](int32_t idx, int buf) {  // the item's slot ids -> s_slots[buf]
+      Item it;
+      decode_item(p, idx, it, false);
+      const int32_t* rp = p.table + static_cast<int64_t>(it.row) * p.table_stride + it.k0;
+      for (int k = lane; k < it.k1 - it.k0; k += 32) cp_async4(smem_u32(s_slots + buf * kMaxChunk + k), rp + k);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    int32_t n = 0, c = 0, buf = 0;
+    int32_t cur = claim();
+    if (cur >= 0) prefetch(cur, 0);
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncwarp();
-    const uint32_t dst = data0 + st * Sh::kStageBytes + (lane < 16 ? 0 : kSlab * RS) + (lane & 15) * RS;
-    bulk_g2s(dst, kv_base + static_cast<int64_t>(slot) * slot_stride, D * 2, bar0 + st * 8);
-  };
+    bool ok = true;
+    while (cur >= 0) {
+      Item it;
+      decode_item(p, cur, it, false);
+      const int32_t nk = it.k1 - it.k0;
+      const int32_t n_slabs = (nk + kSlab - 1) / kSlab;
+      // claim the next item once this one's first stages are issued (its latency then overlaps)
+      const int32_t claim_at = (n_slabs < ns ? n_slabs : ns) - 1;
+      int32_t nxt = -1;
+      const __nv_bfloat16* base = (lane < 16 ? p.k_pool : p.v_pool) + static_cast<int64_t>(it.hg) * p.hpc * D;
+      for (int32_t s = 0; s < n_slabs; ++s, ++c) {
+        const int st = c % ns;
+        if (c >= ns && !mbar_wait(empty0 + 8 * st, ((c / ns) + 1) & 1)) { ok = false; break; }
+        if (*s_abort) { ok = false; break; }
+        if (s == 0 && lane == 0) s_items[n % kItemRing] = cur;
+        if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, 2 * kSlab * row_bytes);
+        __syncwarp();
+        int32_t key = s * kSlab + (lane & 15);
+        key = key < nk ? key : nk - 1;  // rows past the range repeat the last key (finite, weight 0)
+        int32_t slot = s_slots[buf * kMaxChunk + key];
+        if (slot < 0 || slot >= p.num_slots) {
+          flag_error(p.err, RA_DEVERR_SLOT);
+          slot = 0;
+        }
+        const uint32_t dst = stage0 + st * p.stage_bytes + (lane < 16 ? 0 : kSlab * RS) + (lane & 15) * RS;
+        bulk_g2s(dst, base + static_cast<int64_t>(slot) * p.hkv * D, row_bytes, full0 + 8 * st);
+        if (s == claim_at) {
+          nxt = claim();
+          if (nxt >= 0) prefetch(nxt, buf ^ 1);
+        }
+      }
+      if (!ok) break;
+      asm volatile("cp.async.wait_group 0;" ::: "memory");  // the next item's slot ids
+      __syncwarp();
+      ++n;
+      cur = nxt;
+      buf ^= 1;
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (ok) {
+      // end marker: item id -1 published through the next stage
+      const int st = c % ns;
+      if (c >= ns && !mbar_wait(empty0 + 8 * st, ((c / ns) + 1) & 1)) ok = false;
+      if (ok && lane == 0) {
+        s_items[n % kItemRing] = -1;
+        mbar_arrive(full0 + 8 * st);
+      }
+    }
+    if (!ok) {
+      if (lane == 0) {
+        *s_abort = 1;
+        flag_error(p.err, RA_DEVERR_TIMEOUT);
+      }
+      // copies this warp issued must land before the CTA leaves
+      for (int32_t j = (c > ns ? c - ns : 0); j < c; ++j) mbar_wait(full0 + 8 * (j % ns), (j / ns) & 1);
+    }
+    return;
+  }
+  if (warp > nc) return;
 
-  const int32_t n_pro = my_slabs < NSTAGE ? my_slabs : NSTAGE;
-  for (int32_t i = 0; i < n_pro; ++i) issue(i, load_slot(row_ptr, slab_key(i), p.num_slots, p.err));
-
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float acc[KT][4];
-#pragma unroll
-  for (int mt = 0; mt < KT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-
-  // lane's ldmatrix row addresses inside a stage
-  const uint32_t a_off = (lane & 15) * RS + (lane >> 4) * 16;                                  // K, non-transposed
-  const uint32_t v_off = kSlab * RS + ((lane & 7) + ((lane >> 4) << 3)) * RS + ((lane >> 3) & 1) * 16;  // V, transposed
-
-  int32_t i = 0;
-  bool timed_out = false;
-  for (; i < my_slabs; ++i) {
-    const int st = i % NSTAGE;
-    const bool refill = i + NSTAGE < my_slabs;
-    const int32_t next_slot = refill ? load_slot(row_ptr, slab_key(i + NSTAGE), p.num_slots, p.err) : 0;
-    if (!mbar_wait(bar0 + st * 8, (i / NSTAGE) & 1)) {
-      timed_out = true;
+  // ================================================================ consumers
+  const int g = lane >> 2;  // q head within the GQA group (MMA N index)
+  const int tq = lane & 3;
+  const uint32_t a_off = (lane & 15) * RS + (lane >> 4) * 16 + warp * D * 2;
+  const uint32_t v_off = kSlab * RS + ((lane & 7) + ((lane >> 4) << 3)) * RS + ((lane >> 3) & 1) * 16 + warp * D * 2;
+  int32_t n = 0, c = 0;
+  bool clean = false;  // left through the end marker
+  for (;; ++n) {
+    int st = c % ns;
+    if (!mbar_wait(full0 + 8 * st, (c / ns) & 1) || *s_abort) break;
+    const int32_t idx = s_items[n % kItemRing];
+    if (idx < 0) {
+      clean = true;
       break;
     }
-    const uint32_t stage = data0 + st * Sh::kStageBytes;
-
-    // S^T[16 keys x 8 heads] = K Q^T
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    Item it;
+    decode_item(p, idx, it, false);
+    const int kh = it.hg * p.hpc + warp;
+    // Q^T fragments (B operand): column g is q head kh*G + g
+    uint32_t qf[KT][2];
+    {
+      const bool live = g < p.group;
+      const __nv_bfloat16* qrow = p.q + (static_cast<int64_t>(it.b) * p.hq + kh * p.group + (live ? g : 0)) * D;
 #pragma unroll
-    for (int kk = 0; kk < KT; ++kk) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(stage + a_off + kk * 32, a0, a1, a2, a3);
-      mma_bf16_16816(s, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+      for (int kk = 0; kk < KT; ++kk) {
+        qf[kk][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * tq)) : 0u;
+        qf[kk][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * tq)) : 0u;
+      }
     }
-    // mask keys past the range, log2-domain scores
-    const int32_t kbase = k0 + (warp + i * NWARPS) * kSlab;
-    const bool v_lo = kbase + g < k1;
-    const bool v_hi = kbase + g + 8 < k1;
-    const float x0 = v_lo ? s[0] * p.scale_log2 : -INFINITY;
-    const float x1 = v_lo ? s[1] * p.scale_log2 : -INFINITY;
-    const float x2 = v_hi ? s[2] * p.scale_log2 : -INFINITY;
-    const float x3 = v_hi ? s[3] * p.scale_log2 : -INFINITY;
-    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float acc[KT][4];
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+    const int32_t n_slabs = (it.k1 - it.k0 + kSlab - 1) / kSlab;
+    bool ok = true;
+    for (int32_t s = 0; s < n_slabs; ++s, ++c) {
+      st = c % ns;
+      if (s > 0 && !mbar_wait(full0 + 8 * st, (c / ns) & 1)) { ok = false; break; }
+      const uint32_t stage = stage0 + st * p.stage_bytes;
+      // S^T[16 keys x 8 heads] = K Q^T, two independent MMA chains
+      float s1[4] = {0.f, 0.f, 0.f, 0.f};
+      float s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < KT; kk += 2) {
+        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+        ldsm_x4(stage + a_off + kk * 32, a0, a1, a2, a3);
+        ldsm_x4(stage + a_off + (kk + 1) * 32, b0, b1, b2, b3);
+        mma_bf16_16816(s1, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+        mma_bf16_16816(s2, b0, b1, b2, b3, qf[kk + 1][0], qf[kk + 1][1]);
+      }
+      const int32_t kbase = it.k0 + s * kSlab;
+      const bool v_lo = kbase + g < it.k1;
+      const bool v_hi = kbase + g + 8 < it.k1;
+      const float x0 = v_lo ? (s1[0] + s2[0]) * p.scale_log2 : -INFINITY;
+      const float x1 = v_lo ? (s1[1] + s2[1]) * p.scale_log2 : -INFINITY;
+      const float x2 = v_hi ? (s1[2] + s2[2]) * p.scale_log2 : -INFINITY;
+      const float x3 = v_hi ? (s1[3] + s2[3]) * p.scale_log2 : -INFINITY;
+      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      // key 0 of a slab is always in range, so the new maxima are finite
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1), p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
+      l0 = l0 * al0 + p0 + p2;
+      l1 = l1 * al1 + p1 + p3;
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        acc[mt][0] *= al0;
+        acc[mt][1] *= al1;
+        acc[mt][2] *= al0;
+        acc[mt][3] *= al1;
+      }
+      // P^T as the B operand: transpose the two 8x8 key blocks
+      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+      // O^T[D x 8] += V^T P^T
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_trans(stage + v_off + mt * 32, a0, a1, a2, a3);
+        mma_bf16_16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * st);
+    }
+    if (!ok) break;
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     }
-    // key 0 of a slab is always in range, so the new maxima are finite
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1), p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
-    l0 = l0 * al0 + p0 + p2;
-    l1 = l1 * al1 + p1 + p3;
+    // outputs: thread holds (d = mt*16 + g [+8], q head 2*tq [+1]) of this kv head
+    const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+    const bool h0 = 2 * tq < p.group, h1 = 2 * tq + 1 < p.group;
+    const int64_t bh0 = static_cast<int64_t>(it.b) * p.hq + kh * p.group + 2 * tq;
+    if (it.n_splits == 1 && it.start == 0) {
 #pragma unroll
-    for (int mt = 0; mt < KT; ++mt) {
-      acc[mt][0] *= al0;
-      acc[mt][1] *= al1;
-      acc[mt][2] *= al0;
-      acc[mt][3] *= al1;
-    }
-    // P^T as the B operand: transpose the two 8x8 key blocks
-    const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
-    const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
-    // O^T[D x 8] += V^T P^T
-#pragma unroll
-    for (int mt = 0; mt < KT; ++mt) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4_trans(stage + v_off + mt * 32, a0, a1, a2, a3);
-      mma_bf16_16816(acc[mt], a0, a1, a2, a3, pb0, pb1);
-    }
-    __syncwarp();
-    if (refill) {
-      fence_proxy_async_smem();
-      issue(i + NSTAGE, next_slot);
-    }
-  }
-  if (timed_out) {
-    // drain this warp's copies still in flight (bounded), then give up on the CTA
-    const int32_t issued = my_slabs < i + NSTAGE ? my_slabs : i + NSTAGE;
-    for (int32_t j = i; j < issued; ++j) mbar_wait(bar0 + (j % NSTAGE) * 8, (j / NSTAGE) & 1);
-    if (lane == 0) {
-      flag_error(p.err, RA_DEVERR_TIMEOUT);
-      s_abort = 1;
-    }
-  }
-
-  // full row sums: the 8 lanes of a column share m
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-  }
-  __syncthreads();  // every warp's copies are consumed: the stage buffers can be reused
-  if (s_abort) return;
-
-  // ---- merge the warps: smem floats [NWARPS][8] m, [NWARPS][8] l, [NWARPS][D][8] O^T
-  float* fm = reinterpret_cast<float*>(smem + 128);
-  float* fl = fm + NWARPS * 8;
-  float* fo = fl + NWARPS * 8;
-  if (g == 0) {
-    fm[warp * 8 + 2 * tq] = m0;
-    fm[warp * 8 + 2 * tq + 1] = m1;
-    fl[warp * 8 + 2 * tq] = l0;
-    fl[warp * 8 + 2 * tq + 1] = l1;
-  }
-#pragma unroll
-  for (int mt = 0; mt < KT; ++mt) {
-    const int d = mt * 16 + g;
-    float* o = fo + (warp * D + d) * 8 + 2 * tq;
-    o[0] = acc[mt][0];
-    o[1] = acc[mt][1];
-    o[8 * 8] = acc[mt][2];
-    o[8 * 8 + 1] = acc[mt][3];
-  }
-  __syncthreads();
-
-  const bool direct = (n_splits == 1) && (start == 0);
-  for (int idx = threadIdx.x; idx < p.group * D; idx += NWARPS * 32) {
-    const int gg = idx / D;
-    const int d = idx - gg * D;
-    float mm = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NWARPS; ++w) mm = fmaxf(mm, fm[w * 8 + gg]);
-    float ll = 0.f, oo = 0.f;
-#pragma unroll
-    for (int w = 0; w < NWARPS; ++w) {
-      const float mw = fm[w * 8 + gg];
-      if (mw == -INFINITY) continue;
-      const float sc = ex2(mw - mm);
-      ll += fl[w * 8 + gg] * sc;
-      oo += fo[(w * D + d) * 8 + gg] * sc;
-    }
-    const int h = kh * p.group + gg;
-    const int64_t bh = static_cast<int64_t>(b) * p.hq + h;
-    if (direct) {
-      p.o[bh * D + d] = __float2bfloat16_rn(oo / ll);
+      for (int mt = 0; mt < KT; ++mt) {
+        const int d = mt * 16 + g;
+        if (h0) {
+          p.o[bh0 * D + d] = __float2bfloat16_rn(acc[mt][0] * inv0);
+          p.o[bh0 * D + d + 8] = __float2bfloat16_rn(acc[mt][2] * inv0);
+        }
+        if (h1) {
+          p.o[(bh0 + 1) * D + d] = __float2bfloat16_rn(acc[mt][1] * inv1);
+          p.o[(bh0 + 1) * D + d + 8] = __float2bfloat16_rn(acc[mt][3] * inv1);
+        }
+      }
     } else {
-      const int64_t ps = bh * p.max_splits + split;
-      p.part_o[ps * D + d] = oo / ll;
-      if (d == 0) p.part_lse[ps] = mm + __log2f(ll);
+      const int64_t ps0 = bh0 * p.max_splits + it.split;
+      const int64_t ps1 = ps0 + p.max_splits;
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        const int d = mt * 16 + g;
+        if (h0) {
+          p.part_o[ps0 * D + d] = acc[mt][0] * inv0;
+          p.part_o[ps0 * D + d + 8] = acc[mt][2] * inv0;
+        }
+        if (h1) {
+          p.part_o[ps1 * D + d] = acc[mt][1] * inv1;
+          p.part_o[ps1 * D + d + 8] = acc[mt][3] * inv1;
+        }
+      }
+      if (g == 0) {
+        if (h0) p.part_lse[ps0] = m0 + __log2f(l0);
+        if (h1) p.part_lse[ps1] = m1 + __log2f(l1);
+      }
     }
+  }
+  if (!clean && lane == 0) {
+    // a bounded wait ran out: stop the producer as well
+    *s_abort = 1;
+    flag_error(p.err, RA_DEVERR_TIMEOUT);
   }
 }
 
@@ -353,24 +412,20 @@ __global__ void cascade_key_start_kernel(int32_t* key_start, int32_t batch, cons
   }
 }
 
-constexpr int kNWarps = 4;
-constexpr int kNStage = 3;
-
 template <int D>
-ra_status launch_decode(const DecodeParams& p, cudaStream_t stream) {
-  constexpr int smem = decode_smem_bytes<D, kNWarps, kNStage>();
-  auto kern = decode_split_kernel<D, kNWarps, kNStage>;
-  static bool configured[64] = {};
+ra_status launch_decode(const DecodeParams& p, int grid, int smem, cudaStream_t stream) {
+  auto kern = decode_kernel<D>;
+  static int configured[64] = {};
   DeviceInfo dev;
   if (ra_status st = current_device(&dev)) return st;
-  if (!configured[dev.device]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (smem > dev.max_smem_optin) return fail(RA_ERR_UNSUPPORTED, "decode needs %d bytes of shared memory", smem);
+  if (configured[dev.device] < smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaFuncSetAttribute(decode): %s", cudaGetErrorString(e));
-    configured[dev.device] = true;
+    configured[dev.device] = kSmemLimit;
   }
-  dim3 grid(p.max_splits, p.hkv, p.batch);
-  kern<<<grid, kNWarps * 32, smem, stream>>>(p);
-  if (ra_status st = check_launch("decode_split_kernel")) return st;
+  kern<<<grid, 32 * (p.hpc + 1), smem, stream>>>(p);
+  if (ra_status st = check_launch("decode_kernel")) return st;
   const int nwarps = p.batch * p.hq;
   decode_combine_kernel<D><<<(nwarps + 3) / 4, 128, 0, stream>>>(p);
   return check_launch("decode_combine_kernel");
@@ -378,17 +433,26 @@ ra_status launch_decode(const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-// Private keys per split: at least 128, at most 1024, aiming at ~2K (request, kv head, split) work items.
+// kv heads per work item: the largest divisor of Hkv that is <= 8 (one consumer warp each).
+static int32_t heads_per_cta(int32_t num_kv_heads) {
+  for (int32_t h = kMaxHeadsPerCta; h > 1; --h)
+    if (num_kv_heads % h == 0) return h;
+  return 1;
+}
+
+// Private keys per work item: between 256 and 1024, aiming at ~1K (request, split, head group)
+// items over the host-side bound of the batch's keys.
 // Shared-prefix pass (cascade): 128-row tiles of (member, q head) per group and kv head; the prefix is
 // split in multiples of 128 keys until there are about two CTAs per SM of work.
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seq_len,
                        int32_t num_groups, int32_t max_group_prefix_len, int32_t max_group_size) {
   DecodePlan pl;
-  const int64_t work = static_cast<int64_t>(batch) * num_kv_heads * (max_seq_len > 0 ? max_seq_len : 1);
-  int64_t chunk = (work + 2047) / 2048;
+  const int64_t n_hg = num_kv_heads / heads_per_cta(num_kv_heads);
+  const int64_t work = static_cast<int64_t>(batch) * n_hg * (max_seq_len > 0 ? max_seq_len : 1);
+  int64_t chunk = (work + 1023) / 1024;
   chunk = (chunk + 63) / 64 * 64;
-  if (chunk < 128) chunk = 128;
-  if (chunk > 1024) chunk = 1024;
+  if (chunk < 256) chunk = 256;
+  if (chunk > kMaxChunk) chunk = kMaxChunk;
   pl.chunk = static_cast<int32_t>(chunk);
   pl.max_splits = static_cast<int32_t>((static_cast<int64_t>(max_seq_len) + chunk - 1) / chunk);
   if (pl.max_splits < 1) pl.max_splits = 1;
@@ -426,6 +490,8 @@ DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int3
     w.key_start = off;
     off += up(static_cast<size_t>(batch) * sizeof(int32_t));
   }
+  w.counter = off;
+  off += up(sizeof(int32_t));
   w.total = off;
   return w;
 }
@@ -526,5 +592,23 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
     CascadeArgs ca{group_indptr, group_reqs, group_prefix_len, num_groups, max_group_prefix_len, max_group_size};
     if (ra_status st = launch_cascade_prefix(p, ca, head_dim, s)) return st;
   }
-  return head_dim == 128 ? launch_decode<128>(p, s) : launch_decode<64>(p, s);
+  // persistent decode geometry
+  p.hpc = heads_per_cta(num_kv_heads);
+  p.n_hgroups = num_kv_heads / p.hpc;
+  p.row_stride = p.hpc * head_dim * 2 + 16;
+  p.stage_bytes = 2 * 16 * p.row_stride;
+  p.nstage = (kSmemLimit - kHdrBytes) / p.stage_bytes;
+  if (p.nstage > kMaxStages) p.nstage = kMaxStages;
+  if (p.nstage < 2) return fail(RA_ERR_UNSUPPORTED, "decode ring does not fit in shared memory");
+  const int smem = kHdrBytes + p.nstage * p.stage_bytes;
+  const int64_t n_items = static_cast<int64_t>(pl.max_splits) * batch * p.n_hgroups;
+  if (n_items > INT32_MAX / 2) return fail(RA_ERR_UNSUPPORTED, "too many decode work items");
+  p.n_items = static_cast<int32_t>(n_items);
+  p.counter = reinterpret_cast<int32_t*>(ws + wl.counter);
+  DeviceInfo dev;
+  if (ra_status st = current_device(&dev)) return st;
+  const int grid = static_cast<int>(n_items < dev.num_sms ? n_items : dev.num_sms);
+  cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+  return head_dim == 128 ? launch_decode<128>(p, grid, smem, s) : launch_decode<64>(p, grid, smem, s);
 }

@@ -33,6 +33,13 @@ struct DecodeParams {
   const int32_t* key_start;  // [batch] first private position (cascade), or nullptr
   int32_t chunk;             // keys per split
   int32_t max_splits;
+  int32_t hpc;               // kv heads per CTA item (consumer warps)
+  int32_t n_hgroups;         // hkv / hpc
+  int32_t nstage;            // ring stages
+  int32_t row_stride;        // bytes between keys in a ring stage (hpc * D * 2 + 16)
+  int32_t stage_bytes;       // 2 * 16 * row_stride
+  int32_t n_items;           // max_splits * batch * n_hgroups
+  int32_t* counter;          // work-item counter (zeroed before each launch)
   float* part_o;    // [batch, hq, max_splits, D]
   float* part_lse;  // [batch, hq, max_splits] (log2 domain)
   int32_t cchunk;      // shared-prefix keys per prefix-pass split (cascade)
@@ -50,8 +57,10 @@ struct DecodePlan {
 };
 
 struct DecodeWorkspace {
-  size_t part_o = 0, part_lse = 0, casc_o = 0, casc_lse = 0, key_start = 0, total = 0;
+  size_t part_o = 0, part_lse = 0, casc_o = 0, casc_lse = 0, key_start = 0, counter = 0, total = 0;
 };
+
+constexpr int kMaxHeadsPerCta = 8;  // consumer warps of the decode kernel
 
 struct CascadeArgs {
   const int32_t* group_indptr;

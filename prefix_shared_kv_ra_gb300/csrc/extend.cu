@@ -22,7 +22,7 @@ namespace ra {
 
 namespace {
 
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
