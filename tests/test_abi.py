@@ -75,9 +75,10 @@ def test_decode_validation(lib):
 
 def test_decode_workspace_grows_with_bounds(lib):
     a = ra.ra_decode_workspace_bytes(64, 32, 8, 128, 4096)
-    b = ra.ra_decode_workspace_bytes(64, 32, 8, 128, 8192)
+    b = ra.ra_decode_workspace_bytes(64, 32, 8, 128, 512)
     c = ra.ra_decode_workspace_bytes(64, 32, 8, 128, 4096, 8, 1024, 8)
-    assert 0 < a < b and c > a
+    d = ra.ra_decode_workspace_bytes(64, 32, 8, 128, 32768)
+    assert 0 < b < a < c and d >= a
     assert ra.ra_decode_workspace_bytes(0, 32, 8, 128, 4096) == 0
 
 
