@@ -1,9 +1,10 @@
 // attn_tc.cuh -- tcgen05 / TMEM attention tile kernel over the slot pool.
 //
-// One CTA computes 128 query rows of one kv head against a range of keys
-// gathered from the pool through a req_to_token row.  The rows are a GQA
-// block: 128 / G tokens (or decode requests) x the G q heads of the kv head,
-// so every gathered K/V tile feeds 128 rows of tensor-core work.  Two users:
+// One CTA computes 256 query rows of one kv head -- two 128-row tiles, each a
+// GQA block of 128 / G tokens (or decode requests) x the G q heads of the kv
+// head -- against a range of keys gathered from the pool through a
+// req_to_token row.  Every gathered 128-key K/V tile feeds both query tiles,
+// i.e. 256 rows of tensor-core work.  Two users:
 //
 //  * extend (EXTEND = true): rows are suffix tokens of one request; row
 //    (token i, head g) sees keys 0 .. P + i (cached prefix + causal suffix);
@@ -13,18 +14,23 @@
 //    prefix, read once for the whole group; (output, log2-sum-exp) partials
 //    are written for the decode combine pass.
 //
-// Warp roles (288 threads):
-//  warps 0-3  softmax + epilogue, one thread per row = TMEM lane;
-//  warps 4-7  producers: gather K (warps 4,5) and V (warps 6,7) rows of a
-//             128-key tile with 16-byte cp.async into the 128-byte-swizzled
-//             K-major (K) / MN-major (V) layouts tcgen05 reads, completion
-//             signalled on per-stage mbarriers; the query tile of an extend
-//             CTA is one 3-D TMA tile load (cp.async.bulk.tensor) instead;
-//  warp 8     allocates TMEM and issues tcgen05.mma from one thread:
-//             S = Q K^T (SS form, M=128 N=128) into one of two TMEM S buffers,
-//             O += P V (TS form: P read from TMEM where softmax stored it over
-//             its own S buffer) into the TMEM O accumulator.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256+D); 512 allocated.
+// Warp roles (352 threads):
+//  warps 0-3  softmax + epilogue of query tile 0, one thread per row = TMEM lane;
+//  warps 4-7  the same for query tile 1;
+//  warp 8     gathers K rows, warp 9 gathers V rows of each 128-key tile with
+//             16-byte cp.async into the 128-byte-swizzled K-major (K) and
+//             MN-major (V) layouts tcgen05 reads (completion on per-stage
+//             mbarriers); an extend CTA's query tiles arrive by 3-D TMA tile
+//             loads (cp.async.bulk.tensor), a prefix-pass CTA's are gathered
+//             by the same two warps;
+//  warp 10    allocates TMEM and issues tcgen05.mma from one thread, in the
+//             order S0 = Q0 K^T, S1 = Q1 K^T, then per key tile
+//             O0 += P0 V, S0' = Q0 K'^T, O1 += P1 V, S1' = Q1 K'^T, so the
+//             tensor core works on one query tile while the other tile's
+//             softmax warps run (ping-pong).
+// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512); P_i is
+// stored by the softmax warps over the first 64 columns of S_i (bf16 pairs)
+// and read from there by the TS-form MMA.
 //
 // Online softmax in the log2 domain with a lazy rescale: a row's reference
 // maximum moves only when the running maximum exceeds it by more than 8
@@ -77,23 +83,24 @@ struct TcParams {
 
 namespace tc {
 
-constexpr int kRows = 128;     // query rows per CTA (MMA M)
+constexpr int kRows = 128;     // query rows per tile (MMA M)
+constexpr int kTiles = 2;      // query tiles per CTA
 constexpr int kKeys = 128;     // keys per tile (MMA N of S, K of PV)
-constexpr int kThreads = 288;  // 9 warps
-constexpr int kProducerBase = 128;
-constexpr int kMmaWarp = 8;
+constexpr int kThreads = 352;  // 11 warps
+constexpr int kKWarp = 8;
+constexpr int kVWarp = 9;
+constexpr int kMmaWarp = 10;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS1 = 128;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D, int NS>
+template <int D, int KS, int VS>
 struct Layout {
-  static constexpr int kTileBytes = kKeys * D * 2;  // one K or V tile (also the Q tile: 128 rows)
+  static constexpr int kTileBytes = kKeys * D * 2;  // one K or V tile (also one query tile: 128 rows)
   static constexpr int kQ = 0;
-  static constexpr int kK = kTileBytes;
-  static constexpr int kV = kK + NS * kTileBytes;
-  static constexpr int kBytes = kV + NS * kTileBytes;
+  static constexpr int kK = kTiles * kTileBytes;
+  static constexpr int kV = kK + KS * kTileBytes;
+  static constexpr int kBytes = kV + VS * kTileBytes;
   static constexpr int kDynSmem = kBytes + 1024;  // + alignment slack
 };
 
@@ -104,40 +111,34 @@ __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (c >> 3) * (kRows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 __device__ __forceinline__ bool aborted(volatile int* flag) { return *flag != 0; }
 
 }  // namespace tc
 
-template <int D, int NS, bool EXTEND>
+template <int D, int KS, int VS, bool EXTEND>
 __global__ void __launch_bounds__(tc::kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap qmap) {
+    attn_tc_kernel(const __grid_constant__ TcParams p, const __grid_constant__ CUtensorMap qmap,
+                   const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
   using namespace tc;
-  using L = Layout<D, NS>;
-  constexpr int CH = D / 8;  // 16-byte chunks per row
+  using L = Layout<D, KS, VS>;
+  constexpr int NSMAX = KS > VS ? KS : VS;
+  constexpr int HALVES = D / 64;  // 128-byte (64-element) column blocks of a row
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_q, bar_kf[NS], bar_ke[NS], bar_vf[NS], bar_ve[NS], bar_s[2], bar_p[2],
-      bar_o, bar_done;
+  __shared__ __align__(8) uint64_t bar_q, bar_kf[KS], bar_ke[KS], bar_vf[VS], bar_ve[VS], bar_s[kTiles],
+      bar_p[kTiles], bar_o[kTiles], bar_done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.group;
-  const int T = kRows / G;  // tokens (or members) per CTA
+  const int T = kRows / G;  // tokens (or members) per query tile
   const int kh = blockIdx.y;
 
   // ------------------------------------------------------------------ job (CTA-uniform)
   int32_t kbeg = 0, kend = 0, table_row = 0;
-  int32_t n_valid = 0;   // valid tokens / members in this CTA
-  int32_t causal0 = 0;   // extend: key limit of token 0 is causal0 + 1
+  int32_t n_valid = 0;   // valid tokens / members in this CTA (of 2T)
+  int32_t causal0 = 0;   // extend: token t of the CTA sees keys < causal0 + t + 1
   int64_t q_tok0 = 0;    // extend: first q token
   int32_t mem0 = 0;      // cascade: first member index into group_reqs
   int32_t csplit = 0;
@@ -152,27 +153,27 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       E = min(max(E, 0), p.max_extend_len);
       if (P < 0 || P > p.max_prefix_len) return;
     }
-    if (tile * T >= E) return;
+    if (tile * kTiles * T >= E) return;
     if (table_row < 0 || table_row >= p.table_rows) {
       if (tile == 0 && kh == 0 && threadIdx.x == 0) flag_error(p.err, RA_DEVERR_TABLE);
       return;
     }
-    n_valid = min(T, E - tile * T);
-    causal0 = P + tile * T;
+    n_valid = min(kTiles * T, E - tile * kTiles * T);
+    causal0 = P + tile * kTiles * T;
     kbeg = 0;
     kend = causal0 + n_valid;
     if (kend > p.table_stride) {
       if (tile == 0 && kh == 0 && threadIdx.x == 0) flag_error(p.err, RA_DEVERR_LENGTH);
       return;
     }
-    q_tok0 = static_cast<int64_t>(__ldg(p.qo_indptr + b)) + tile * T;
+    q_tok0 = static_cast<int64_t>(__ldg(p.qo_indptr + b)) + tile * kTiles * T;
   } else {
     const int g = blockIdx.z;
     const int32_t m_begin = __ldg(p.group_indptr + g);
     const int32_t n_mem = __ldg(p.group_indptr + g + 1) - m_begin;
     const int mt = blockIdx.x / p.max_csplits;
     csplit = blockIdx.x - mt * p.max_csplits;
-    if (mt * T >= n_mem) return;
+    if (mt * kTiles * T >= n_mem) return;
     const int32_t Pg = __ldg(p.group_prefix_len + g);
     if (Pg < 1 || Pg > p.max_seq_len) {
       if (blockIdx.x == 0 && kh == 0 && threadIdx.x == 0) flag_error(p.err, RA_DEVERR_LENGTH);
@@ -181,8 +182,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     if (csplit * p.cchunk >= Pg) return;
     kbeg = csplit * p.cchunk;
     kend = min(Pg, kbeg + p.cchunk);
-    mem0 = m_begin + mt * T;
-    n_valid = min(T, n_mem - mt * T);
+    mem0 = m_begin + mt * kTiles * T;
+    n_valid = min(kTiles * T, n_mem - mt * kTiles * T);
     const int32_t leader = __ldg(p.group_reqs + m_begin);
     if (leader < 0 || leader >= p.batch) {
       if (blockIdx.x == 0 && kh == 0 && threadIdx.x == 0) flag_error(p.err, RA_DEVERR_TABLE);
@@ -199,24 +200,26 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase + L::kQ;
+  auto sQ = [&](int i) { return sbase + L::kQ + i * L::kTileBytes; };
   auto sK = [&](int st) { return sbase + L::kK + st * L::kTileBytes; };
   auto sV = [&](int st) { return sbase + L::kV + st * L::kTileBytes; };
 
   if (threadIdx.x == 0) {
     s_abort = 0;
-    mbar_init(smem_u32(&bar_q), EXTEND ? 1 : 128);
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(smem_u32(&bar_kf[s]), 64);
-      mbar_init(smem_u32(&bar_vf[s]), 64);
+    mbar_init(smem_u32(&bar_q), 1);
+    for (int s = 0; s < KS; ++s) {
+      mbar_init(smem_u32(&bar_kf[s]), 1);
       mbar_init(smem_u32(&bar_ke[s]), 1);
+    }
+    for (int s = 0; s < VS; ++s) {
+      mbar_init(smem_u32(&bar_vf[s]), 1);
       mbar_init(smem_u32(&bar_ve[s]), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&bar_s[s]), 1);
-      mbar_init(smem_u32(&bar_p[s]), 128);
+    for (int i = 0; i < kTiles; ++i) {
+      mbar_init(smem_u32(&bar_s[i]), 1);
+      mbar_init(smem_u32(&bar_p[i]), 128);
+      mbar_init(smem_u32(&bar_o[i]), 1);
     }
-    mbar_init(smem_u32(&bar_o), 1);
     mbar_init(smem_u32(&bar_done), 1);
     fence_mbar_init();
   }
@@ -234,74 +237,94 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     flag_error(p.err, RA_DEVERR_TIMEOUT);
   };
 
-  if (warp >= 4 && warp < 8) {
-    // ================================================================ producers
-    const int ptid = threadIdx.x - kProducerBase;
-    const int pw = ptid >> 5;
-    const bool is_v = pw >= 2;
-    const int half = pw & 1;
-    // ---- query tile
-    if constexpr (EXTEND) {
-      if (ptid == 0) {
-        prefetch_tensormap(&qmap);
-        const uint32_t bq = smem_u32(&bar_q);
-        mbar_arrive_expect_tx(bq, kRows * D * 2);
+  if (warp == kKWarp || warp == kVWarp) {
+    // ================================================================ producers (TMA)
+    const bool is_v = warp == kVWarp;
+    const CUtensorMap* map = is_v ? &vmap : &kmap;
+    if (lane == 0) prefetch_tensormap(map);
+    // ---- query tiles (K warp)
+    if (warp == kKWarp) {
+      const uint32_t bq = smem_u32(&bar_q);
+      if constexpr (EXTEND) {
+        if (lane == 0) {
+          prefetch_tensormap(&qmap);
+          mbar_arrive_expect_tx(bq, kTiles * kRows * D * 2);
 #pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-          asm volatile(
-              "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-              " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sQ + h * (kRows * 128)),
-              "l"(&qmap), "r"(h * 64), "r"(kh * G), "r"(static_cast<int32_t>(q_tok0)), "r"(bq)
-              : "memory");
+          for (int i = 0; i < kTiles; ++i) {
+#pragma unroll
+            for (int h = 0; h < HALVES; ++h) {
+              asm volatile(
+                  "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                  " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sQ(i) + h * (kRows * 128)),
+                  "l"(&qmap), "r"(h * 64), "r"(kh * G), "r"(static_cast<int32_t>(q_tok0 + i * T)), "r"(bq)
+                  : "memory");
+            }
+          }
+        }
+      } else {
+        // the members' decode query rows, gathered 4 rows per TMA: CTA row R = (member R / G, q head kh*G + R % G)
+        if (lane == 0) mbar_arrive_expect_tx(bq, kTiles * kRows * D * 2);
+        __syncwarp();
+        for (int grp = lane; grp < kTiles * kRows / 4; grp += 32) {
+          int32_t qrow[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int R = grp * 4 + e;
+            const int k = R / G;
+            int32_t b = __ldg(p.group_reqs + mem0 + (k < n_valid ? k : 0));
+            b = (b < 0 || b >= p.batch) ? 0 : b;
+            qrow[e] = b * p.hq + kh * G + (R % G);
+          }
+          const int R0 = grp * 4;
+#pragma unroll
+          for (int h = 0; h < HALVES; ++h)
+            tma_gather4(sQ(R0 >> 7) + h * (kRows * 128) + (R0 & 127) * 128, &qmap, h * 64, qrow[0], qrow[1], qrow[2],
+                        qrow[3], bq);
         }
       }
-    } else {
-      // gather the members' decode query rows: row r = (member r / G, q head kh*G + r % G)
-      constexpr int RPI = 32 / CH;  // rows per warp instruction
-      for (int it = 0; it < kRows * CH / 128; ++it) {
-        const int r = (it * 4 + pw) * RPI + lane / CH;
-        const int c = lane % CH;
-        const int k = r / G;
-        const int32_t m = mem0 + (k < n_valid ? k : 0);
-        int32_t b = __ldg(p.group_reqs + m);
-        b = (b < 0 || b >= p.batch) ? 0 : b;
-        const __nv_bfloat16* src = p.q + (static_cast<int64_t>(b) * p.hq + kh * G + (r % G)) * D + c * 8;
-        cp_async16(sQ + swz(r, c), src);
-      }
-      cp_async_arrive_noinc(smem_u32(&bar_q));
     }
-    // ---- K / V tiles
-    const __nv_bfloat16* pool = (is_v ? p.v_pool : p.k_pool) + static_cast<int64_t>(kh) * D;
-    const int64_t slot_stride = static_cast<int64_t>(p.hkv) * D;
+    // ---- K (warp 8) or V (warp 9) tiles: lane l gathers keys 4l .. 4l+3 of each 128-key tile.
+    // The slot ids of tile j+1 are loaded while tile j is issued (their latency leaves the issue path).
     uint64_t* full = is_v ? bar_vf : bar_kf;
     uint64_t* empty = is_v ? bar_ve : bar_ke;
-    constexpr int RPI = 32 / CH;
+    const int ns = is_v ? VS : KS;
+    auto load_rows = [&](int j, int32_t (&rowc)[4]) {  // tensor-map row of each key: slot * Hkv + kh
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int32_t key = kbeg + j * kKeys + lane * 4 + e;  // keys past the range repeat the last key
+        int32_t s = __ldg(row_ptr + min(key, kend - 1));
+        if (s < 0 || s >= p.num_slots) {
+          flag_error(p.err, RA_DEVERR_SLOT);
+          s = 0;
+        }
+        rowc[e] = s * p.hkv + kh;
+      }
+    };
+    int issued = 0;
+    int32_t cur[4], nxt[4];
+    load_rows(0, cur);
     for (int j = 0; j < nt; ++j) {
       if (aborted(abort_flag)) break;
-      const int st = j % NS;
-      // slots of this warp's 64 keys (keys past the range repeat the last key: finite, masked)
-      const int32_t key_a = kbeg + j * kKeys + half * 64 + lane;
-      int32_t slot_a = __ldg(row_ptr + min(key_a, kend - 1));
-      int32_t slot_b = __ldg(row_ptr + min(key_a + 32, kend - 1));
-      if (slot_a < 0 || slot_a >= p.num_slots) { flag_error(p.err, RA_DEVERR_SLOT); slot_a = 0; }
-      if (slot_b < 0 || slot_b >= p.num_slots) { flag_error(p.err, RA_DEVERR_SLOT); slot_b = 0; }
-      if (j >= NS && !mbar_wait(smem_u32(&empty[st]), ((j / NS) + 1) & 1)) {
+      const int st = j % ns;
+      if (j + 1 < nt) load_rows(j + 1, nxt);
+      if (j >= ns && !mbar_wait(smem_u32(&empty[st]), ((j / ns) + 1) & 1)) {
         give_up();
         break;
       }
       const uint32_t tile = is_v ? sV(st) : sK(st);
-#pragma unroll 4
-      for (int it = 0; it < 64 / RPI; ++it) {
-        const int rl = it * RPI + lane / CH;  // 0..63
-        const int c = lane % CH;
-        const int32_t sa = __shfl_sync(0xffffffffu, slot_a, rl & 31);
-        const int32_t sb = __shfl_sync(0xffffffffu, slot_b, rl & 31);
-        const int32_t slot = rl < 32 ? sa : sb;
-        cp_async16(tile + swz(half * 64 + rl, c), pool + static_cast<int64_t>(slot) * slot_stride + c * 8);
-      }
-      cp_async_arrive_noinc(smem_u32(&full[st]));
+      if (lane == 0) mbar_arrive_expect_tx(smem_u32(&full[st]), kKeys * D * 2);
+      __syncwarp();
+#pragma unroll
+      for (int h = 0; h < HALVES; ++h)
+        tma_gather4(tile + h * (kRows * 128) + lane * 4 * 128, map, h * 64, cur[0], cur[1], cur[2], cur[3],
+                    smem_u32(&full[st]));
+      issued = j + 1;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) cur[e] = nxt[e];
     }
-    cp_async_wait_all();
+    // copies this warp issued land before the CTA can leave (normally consumed already)
+    for (int j = (issued > ns ? issued - ns : 0); j < issued; ++j)
+      mbar_wait(smem_u32(&full[j % ns]), (j / ns) & 1);
   } else if (warp == kMmaWarp) {
     // ================================================================ MMA issuer
     if (lane == 0) {
@@ -311,40 +334,46 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_after();
       bool issued = false;
-      auto issue_qk = [&](int j) -> bool {
-        const int st = j % NS;
-        if (!mbar_wait(smem_u32(&bar_kf[st]), (j / NS) & 1)) return false;
-        fence_proxy_async_smem();
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + (j & 1) * kColS1;
+      auto qk = [&](int i, int j) -> bool {  // S_i = Q_i K_j^T
+        const int st = j % KS;
+        if (i == 0) {
+          if (!mbar_wait(smem_u32(&bar_kf[st]), (j / KS) & 1)) return false;
+          fence_proxy_async_smem();
+          tc_fence_after();
+        }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (kRows * 128) + (kk & 3) * 32;
-          tc_mma_ss(d_tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK(st) + off, 16, 1024), idesc_qk,
-                    kk > 0);
+          tc_mma_ss(tmem + i * kKeys, sdesc_sw128(sQ(i) + off, 16, 1024), sdesc_sw128(sK(st) + off, 16, 1024),
+                    idesc_qk, kk > 0);
         }
-        tc_commit(smem_u32(&bar_s[j & 1]));
-        tc_commit(smem_u32(&bar_ke[st]));
+        tc_commit(smem_u32(&bar_s[i]));
+        if (i == kTiles - 1) tc_commit(smem_u32(&bar_ke[st]));
         issued = true;
         return true;
       };
-      if (ok) ok = issue_qk(0);
-      for (int j = 0; ok && j < nt; ++j) {
-        if (aborted(abort_flag)) { ok = false; break; }
-        if (j + 1 < nt && !issue_qk(j + 1)) { ok = false; break; }
-        if (!mbar_wait(smem_u32(&bar_p[j & 1]), (j >> 1) & 1)) { ok = false; break; }
+      auto pv = [&](int i, int j) -> bool {  // O_i += P_i V_j
+        const int st = j % VS;
+        if (!mbar_wait(smem_u32(&bar_p[i]), j & 1)) return false;
         tc_fence_after();
-        const int st = j % NS;
-        if (!mbar_wait(smem_u32(&bar_vf[st]), (j / NS) & 1)) { ok = false; break; }
-        fence_proxy_async_smem();
-        tc_fence_after();
+        if (i == 0) {
+          if (!mbar_wait(smem_u32(&bar_vf[st]), (j / VS) & 1)) return false;
+          fence_proxy_async_smem();
+          tc_fence_after();
+        }
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
-          tc_mma_ts(tmem + kColO, tmem + (j & 1) * kColS1 + kk * 8,
+          tc_mma_ts(tmem + kColO + i * 128, tmem + i * kKeys + kk * 8,
                     sdesc_sw128(sV(st) + kk * 2048, kRows * 128, 1024), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(smem_u32(&bar_ve[st]));
-        tc_commit(smem_u32(&bar_o));
+        tc_commit(smem_u32(&bar_o[i]));
+        if (i == kTiles - 1) tc_commit(smem_u32(&bar_ve[st]));
+        return true;
+      };
+      ok = ok && qk(0, 0) && qk(1, 0);
+      for (int j = 0; ok && j < nt; ++j) {
+        if (aborted(abort_flag)) { ok = false; break; }
+        ok = pv(0, j) && (j + 1 >= nt || qk(0, j + 1)) && pv(1, j) && (j + 1 >= nt || qk(1, j + 1));
       }
       if (!ok) give_up();
       if (issued) {
@@ -354,10 +383,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ================================================================ softmax (warps 0-3)
-    const int r = threadIdx.x;  // row = TMEM lane
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-    const int tok = r / G;
+    // ================================================================ softmax (warps 0-7)
+    const int ti = warp >> 2;              // query tile
+    const int r = threadIdx.x & 127;        // row of the tile = TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t col_s = ti * kKeys;
+    const uint32_t col_o = kColO + ti * 128;
+    const int tok = ti * T + r / G;         // token / member of the CTA
     const bool row_valid = tok < n_valid;
     int32_t lim;  // exclusive key limit of this row
     if constexpr (EXTEND) lim = row_valid ? causal0 + tok + 1 : kend;
@@ -365,15 +397,14 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      const int sb = j & 1;
-      const bool fail_here = aborted(abort_flag) || !mbar_wait(smem_u32(&bar_s[sb]), (j >> 1) & 1);
+      const bool fail_here = aborted(abort_flag) || !mbar_wait(smem_u32(&bar_s[ti]), j & 1);
       if (__any_sync(0xffffffffu, fail_here)) { ok = false; break; }  // warp-uniform: tcgen05.ld/st are collective
       tc_fence_after();
       uint32_t sr[kKeys];
 #pragma unroll
       for (int c = 0; c < kKeys / 32; ++c) {
         uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]);
-        tmem_ld32(tmem + lane_addr + sb * kColS1 + c * 32, chunk);
+        tmem_ld32(tmem + lane_addr + col_s + c * 32, chunk);
       }
       tc_wait_ld();
       const int32_t key0 = kbeg + j * kKeys;
@@ -413,36 +444,36 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
           sum8[(2 * e + 1) & 7] += p1;
           pk[e] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(tmem + lane_addr + sb * kColS1 + c * 16, pk);
+        tmem_st16(tmem + lane_addr + col_s + c * 16, pk);
       }
       const float rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       l = l * alpha + rowsum;
       if (j > 0) {
         // Observe PV_{j-1} before releasing P_j: bar_o then never runs two phases ahead of
         // this warp's parity waits, and O is complete for tile j-1 if it must be rescaled.
-        const bool late = !mbar_wait(smem_u32(&bar_o), (j - 1) & 1);
+        const bool late = !mbar_wait(smem_u32(&bar_o[ti]), (j - 1) & 1);
         if (__any_sync(0xffffffffu, late)) { ok = false; break; }
         if (__any_sync(0xffffffffu, resc)) {
           tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t ov[32];
-            tmem_ld32(tmem + lane_addr + kColO + c * 32, ov);
+            tmem_ld32(tmem + lane_addr + col_o + c * 32, ov);
             tc_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32(tmem + lane_addr + kColO + c * 32, ov);
+            tmem_st32(tmem + lane_addr + col_o + c * 32, ov);
           }
         }
       }
       m_used = m_ref;
       tc_wait_st();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bar_p[sb]));
+      mbar_arrive(smem_u32(&bar_p[ti]));
     }
     if (!ok) give_up();
     // ---- epilogue: O / l
-    ok = ok && mbar_wait(smem_u32(&bar_o), (nt - 1) & 1);
+    ok = ok && mbar_wait(smem_u32(&bar_o[ti]), (nt - 1) & 1);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const float inv_l = 1.f / l;
@@ -451,7 +482,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
-          tmem_ld32(tmem + lane_addr + kColO + c * 32, ov);
+          tmem_ld32(tmem + lane_addr + col_o + c * 32, ov);
           tc_wait_ld();
           uint32_t pk[16];
 #pragma unroll
@@ -471,7 +502,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
-          tmem_ld32(tmem + lane_addr + kColO + c * 32, ov);
+          tmem_ld32(tmem + lane_addr + col_o + c * 32, ov);
           tc_wait_ld();
           if (write) {
             float4* d4 = reinterpret_cast<float4*>(dst + c * 32);

@@ -458,8 +458,8 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
   if (pl.max_splits < 1) pl.max_splits = 1;
   if (num_groups > 0 && max_group_prefix_len > 0) {
     const int32_t group = num_q_heads / num_kv_heads;
-    const int32_t rows_per_tile = 128 / (group > 0 ? group : 1);
-    const int64_t mtiles = (max_group_size + rows_per_tile - 1) / rows_per_tile;
+    const int32_t members_per_cta = 2 * (128 / (group > 0 ? group : 1));  // two 128-row query tiles
+    const int64_t mtiles = (max_group_size + members_per_cta - 1) / members_per_cta;
     const int64_t base = static_cast<int64_t>(num_groups) * num_kv_heads * mtiles;
     const int64_t key_tiles = (max_group_prefix_len + 127) / 128;
     int64_t want = (304 + base - 1) / base;

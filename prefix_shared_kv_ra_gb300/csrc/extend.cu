@@ -22,7 +22,11 @@ namespace ra {
 
 namespace {
 
-constexpr int kStages = 3;
+// K ring / V ring depths: the tensor core waits on K first, so K gets the deeper ring.
+template <int D>
+constexpr int k_stages() { return D == 128 ? 3 : 4; }
+template <int D>
+constexpr int v_stages() { return D == 128 ? 2 : 4; }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -38,6 +42,23 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// 2-D view [rows, head_dim] of a bf16 array whose rows are head_dim contiguous elements, read as
+// one 64-element (128-byte, 128B-swizzled) column block of 1 row: the box a TMA gather4 takes.
+ra_status row_gather_map(CUtensorMap* map, const void* base, int64_t rows, int32_t head_dim) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (rows <= 0 || rows > INT32_MAX) return fail(RA_ERR_UNSUPPORTED, "%lld rows exceed a TMA row coordinate", (long long)rows);
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t elem[2] = {1, 1};
+  CUresult cr = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled(rows) failed (%d)", static_cast<int>(cr));
+  return RA_OK;
+}
+
 template <typename Kern>
 ra_status set_smem(Kern kern, int bytes, bool* configured, int device) {
   if (configured[device]) return RA_OK;
@@ -49,8 +70,11 @@ ra_status set_smem(Kern kern, int bytes, bool* configured, int device) {
 
 template <int D>
 ra_status launch_extend(const TcParams& p, const CUtensorMap& qmap, int max_tiles, int batch, cudaStream_t s) {
-  using L = tc::Layout<D, kStages>;
-  auto kern = attn_tc_kernel<D, kStages, true>;
+  CUtensorMap kmap, vmap;
+  if (ra_status st = row_gather_map(&kmap, p.k_pool, p.num_slots * p.hkv, D)) return st;
+  if (ra_status st = row_gather_map(&vmap, p.v_pool, p.num_slots * p.hkv, D)) return st;
+  using L = tc::Layout<D, k_stages<D>(), v_stages<D>()>;
+  auto kern = attn_tc_kernel<D, k_stages<D>(), v_stages<D>(), true>;
   static bool configured[64] = {};
   DeviceInfo dev;
   if (ra_status st = current_device(&dev)) return st;
@@ -58,23 +82,26 @@ ra_status launch_extend(const TcParams& p, const CUtensorMap& qmap, int max_tile
     return fail(RA_ERR_UNSUPPORTED, "extend kernel needs %d bytes of shared memory", L::kDynSmem);
   if (ra_status st = set_smem(kern, L::kDynSmem, configured, dev.device)) return st;
   dim3 grid(max_tiles, p.hkv, batch);
-  kern<<<grid, tc::kThreads, L::kDynSmem, s>>>(p, qmap);
+  kern<<<grid, tc::kThreads, L::kDynSmem, s>>>(p, qmap, kmap, vmap);
   return check_launch("attn_tc_kernel<extend>");
 }
 
 template <int D>
 ra_status launch_prefix(const TcParams& p, int grid_x, int num_groups, cudaStream_t s) {
-  using L = tc::Layout<D, kStages>;
-  auto kern = attn_tc_kernel<D, kStages, false>;
+  using L = tc::Layout<D, k_stages<D>(), v_stages<D>()>;
+  auto kern = attn_tc_kernel<D, k_stages<D>(), v_stages<D>(), false>;
   static bool configured[64] = {};
   DeviceInfo dev;
   if (ra_status st = current_device(&dev)) return st;
   if (L::kDynSmem > dev.max_smem_optin)
     return fail(RA_ERR_UNSUPPORTED, "prefix kernel needs %d bytes of shared memory", L::kDynSmem);
   if (ra_status st = set_smem(kern, L::kDynSmem, configured, dev.device)) return st;
-  CUtensorMap unused{};
+  CUtensorMap qmap, kmap, vmap;
+  if (ra_status st = row_gather_map(&qmap, p.q, static_cast<int64_t>(p.batch) * p.hq, D)) return st;
+  if (ra_status st = row_gather_map(&kmap, p.k_pool, p.num_slots * p.hkv, D)) return st;
+  if (ra_status st = row_gather_map(&vmap, p.v_pool, p.num_slots * p.hkv, D)) return st;
   dim3 grid(grid_x, p.hkv, num_groups);
-  kern<<<grid, tc::kThreads, L::kDynSmem, s>>>(p, unused);
+  kern<<<grid, tc::kThreads, L::kDynSmem, s>>>(p, qmap, kmap, vmap);
   return check_launch("attn_tc_kernel<cascade prefix>");
 }
 
@@ -107,8 +134,8 @@ ra_status launch_cascade_prefix(const DecodeParams& d, const CascadeArgs& ca, in
   p.max_csplits = d.max_csplits;
   p.casc_o = d.casc_o;
   p.casc_lse = d.casc_lse;
-  const int rows_per_tile = 128 / d.group;
-  const int mtiles = (ca.max_group_size + rows_per_tile - 1) / rows_per_tile;
+  const int members_per_cta = tc::kTiles * (128 / d.group);
+  const int mtiles = (ca.max_group_size + members_per_cta - 1) / members_per_cta;
   const int grid_x = mtiles * d.max_csplits;
   return head_dim == 128 ? launch_prefix<128>(p, grid_x, ca.num_groups, stream)
                          : launch_prefix<64>(p, grid_x, ca.num_groups, stream);
@@ -187,7 +214,8 @@ extern "C" ra_status ra_extend_attention(const void* k_pool, const void* v_pool,
   p.max_extend_len = max_extend_len;
   p.max_prefix_len = max_prefix_len;
   p.o = static_cast<__nv_bfloat16*>(o);
-  const int max_tiles = (max_extend_len + rows_per_tile - 1) / rows_per_tile;
+  const int tokens_per_cta = tc::kTiles * rows_per_tile;
+  const int max_tiles = (max_extend_len + tokens_per_cta - 1) / tokens_per_cta;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return head_dim == 128 ? launch_extend<128>(p, qmap, max_tiles, batch, s)
                          : launch_extend<64>(p, qmap, max_tiles, batch, s);
