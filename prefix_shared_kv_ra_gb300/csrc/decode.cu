@@ -341,8 +341,10 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + 1), 1) decode_kernel(c
   }
 }
 
-// Merge per-split partials (and the shared-prefix partial of a cascade member).
-// One warp per (request, q head); each lane owns D/32 output dims.
+// Merge the partials of every request that has more than one (the shared-prefix pass's and the
+// private splits'): o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M).  One warp per (request, q head);
+// lanes load the log-sum-exps 32 at a time (split base + k on lane k), reduce the maximum and the
+// weights with shuffles, then stream the partial rows with independent loads, each lane owning D/32 dims.
 template <int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
   constexpr int V = D / 32;
@@ -357,59 +359,43 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
   int32_t start = p.key_start ? __ldg(p.key_start + b) : 0;
   start = start < 0 ? 0 : (start > L ? L : start);
   const int32_t n_splits = (L - start + p.chunk - 1) / p.chunk;
-  const bool has_prefix = start > 0;
-  if (n_splits == 1 && !has_prefix) return;  // written directly by the split kernel
+  const int32_t n_pre = start > 0 ? (start + p.cchunk - 1) / p.cchunk : 0;
+  if (n_splits == 1 && n_pre == 0) return;  // written directly by the decode kernel
+  const int32_t n = n_pre + n_splits;
   const int64_t bh = warp_global;
-  const int32_t n_pre = has_prefix ? (start + p.cchunk - 1) / p.cchunk : 0;  // prefix-pass splits
+  auto lse_of = [&](int s) {
+    return s < n_pre ? p.casc_lse[bh * p.max_csplits + s] : p.part_lse[bh * p.max_splits + (s - n_pre)];
+  };
   float mm = -INFINITY;
-  for (int s = 0; s < n_pre; ++s) mm = fmaxf(mm, p.casc_lse[bh * p.max_csplits + s]);
-  for (int s = 0; s < n_splits; ++s) mm = fmaxf(mm, p.part_lse[bh * p.max_splits + s]);
+  for (int base = 0; base < n; base += 32)
+    if (base + lane < n) mm = fmaxf(mm, lse_of(base + lane));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
   float acc[V];
-  float wsum = 0.f;
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
-  for (int s = 0; s < n_pre; ++s) {
-    const int64_t ps = bh * p.max_csplits + s;
-    const float w = ex2(p.casc_lse[ps] - mm);
-    wsum += w;
-    const float* src = p.casc_o + ps * D + lane * V;
+  float wsum = 0.f;
+  for (int base = 0; base < n; base += 32) {
+    const int cnt = n - base < 32 ? n - base : 32;
+    const float wl = lane < cnt ? ex2(lse_of(base + lane) - mm) : 0.f;  // weight of split base + lane
+    wsum += wl;
+#pragma unroll 4
+    for (int k = 0; k < cnt; ++k) {
+      const int s = base + k;
+      const float w = __shfl_sync(0xffffffffu, wl, k);
+      const float* src = s < n_pre ? p.casc_o + (bh * p.max_csplits + s) * D
+                                   : p.part_o + (bh * p.max_splits + (s - n_pre)) * D;
 #pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] += w * src[v];
+      for (int v = 0; v < V; ++v) acc[v] += w * src[lane * V + v];
+    }
   }
-  for (int s = 0; s < n_splits; ++s) {
-    const int64_t ps = bh * p.max_splits + s;
-    const float w = ex2(p.part_lse[ps] - mm);
-    wsum += w;
-    const float* src = p.part_o + ps * D + lane * V;
 #pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] += w * src[v];
-  }
+  for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
   const float inv = 1.f / wsum;
 #pragma unroll
-  for (int v = 0; v < V; v += 2) {
-    __nv_bfloat162 pr = __floats2bfloat162_rn(acc[v] * inv, acc[v + 1] * inv);
-    *reinterpret_cast<__nv_bfloat162*>(p.o + bh * D + lane * V + v) = pr;
-  }
-}
-
-// key_start[b] = prefix length of b's cascade group (0 for requests in no group).
-__global__ void cascade_key_start_kernel(int32_t* key_start, int32_t batch, const int32_t* group_indptr,
-                                         const int32_t* group_reqs, const int32_t* group_prefix_len,
-                                         int32_t num_groups, uint32_t* err) {
-  const int32_t total = __ldg(group_indptr + num_groups);
-  for (int32_t m = blockIdx.x * blockDim.x + threadIdx.x; m < total; m += gridDim.x * blockDim.x) {
-    int32_t lo = 0, hi = num_groups;  // group g with indptr[g] <= m < indptr[g+1]
-    while (hi - lo > 1) {
-      const int32_t mid = (lo + hi) >> 1;
-      if (__ldg(group_indptr + mid) <= m) lo = mid; else hi = mid;
-    }
-    const int32_t b = __ldg(group_reqs + m);
-    if (b < 0 || b >= batch) {
-      flag_error(err, RA_DEVERR_TABLE);
-      continue;
-    }
-    key_start[b] = __ldg(group_prefix_len + lo);
-  }
+  for (int v = 0; v < V; v += 2)
+    *reinterpret_cast<__nv_bfloat162*>(p.o + bh * D + lane * V + v) =
+        __floats2bfloat162_rn(acc[v] * inv, acc[v + 1] * inv);
 }
 
 template <int D>
@@ -472,8 +458,8 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
   return pl;
 }
 
-DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int32_t head_dim,
-                                        const DecodePlan& pl, bool cascade) {
+DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, const DecodePlan& pl, bool cascade) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   DecodeWorkspace w;
   const size_t bh = static_cast<size_t>(batch) * num_q_heads;
@@ -487,11 +473,11 @@ DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int3
     off += up(bh * pl.max_csplits * head_dim * sizeof(float));
     w.casc_lse = off;
     off += up(bh * pl.max_csplits * sizeof(float));
-    w.key_start = off;
-    off += up(static_cast<size_t>(batch) * sizeof(int32_t));
   }
-  w.counter = off;
-  off += up(sizeof(int32_t));
+  w.ints = off;
+  (void)num_kv_heads;
+  w.ints_bytes = (static_cast<size_t>(batch) + 1) * sizeof(int32_t);
+  off += up(w.ints_bytes);
   w.total = off;
   return w;
 }
@@ -505,7 +491,7 @@ extern "C" size_t ra_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, 
   if (num_groups > 0 && (max_group_prefix_len <= 0 || max_group_size <= 0)) return 0;
   const ra::DecodePlan pl = ra::plan_decode(batch, num_q_heads, num_kv_heads, max_seq_len, num_groups,
                                             max_group_prefix_len, max_group_size);
-  return ra::layout_decode_workspace(batch, num_q_heads, head_dim, pl, num_groups > 0).total;
+  return ra::layout_decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, pl, num_groups > 0).total;
 }
 
 extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool, int64_t num_slots,
@@ -547,7 +533,7 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
   }
   const DecodePlan pl = plan_decode(batch, num_q_heads, num_kv_heads, max_seq_len, num_groups,
                                     max_group_prefix_len, max_group_size);
-  const DecodeWorkspace wl = layout_decode_workspace(batch, num_q_heads, head_dim, pl, num_groups > 0);
+  const DecodeWorkspace wl = layout_decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, pl, num_groups > 0);
   if (workspace_bytes < wl.total)
     return fail(RA_ERR_WORKSPACE, "workspace of %zu bytes, need %zu", workspace_bytes, wl.total);
   RA_REQUIRE(workspace && aligned16(workspace), "workspace must be non-null and 16-byte aligned");
@@ -577,18 +563,16 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
   p.err = device_error;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
+  int32_t* ints = reinterpret_cast<int32_t*>(ws + wl.ints);
+  p.counter = ints + batch;
+  cudaError_t e = cudaMemsetAsync(ints, 0, wl.ints_bytes, s);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
   if (num_groups > 0) {
     p.cchunk = pl.cchunk;
     p.max_csplits = pl.max_csplits;
     p.casc_o = reinterpret_cast<float*>(ws + wl.casc_o);
     p.casc_lse = reinterpret_cast<float*>(ws + wl.casc_lse);
-    int32_t* key_start = reinterpret_cast<int32_t*>(ws + wl.key_start);
-    p.key_start = key_start;
-    cudaError_t e = cudaMemsetAsync(key_start, 0, sizeof(int32_t) * batch, s);
-    if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
-    cascade_key_start_kernel<<<(batch + 127) / 128, 128, 0, s>>>(key_start, batch, group_indptr, group_reqs,
-                                                                  group_prefix_len, num_groups, device_error);
-    if (ra_status st = check_launch("cascade_key_start_kernel")) return st;
+    p.key_start = ints;  // written by the prefix pass for every member (0 for other requests)
     CascadeArgs ca{group_indptr, group_reqs, group_prefix_len, num_groups, max_group_prefix_len, max_group_size};
     if (ra_status st = launch_cascade_prefix(p, ca, head_dim, s)) return st;
   }
@@ -604,11 +588,8 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
   const int64_t n_items = static_cast<int64_t>(pl.max_splits) * batch * p.n_hgroups;
   if (n_items > INT32_MAX / 2) return fail(RA_ERR_UNSUPPORTED, "too many decode work items");
   p.n_items = static_cast<int32_t>(n_items);
-  p.counter = reinterpret_cast<int32_t*>(ws + wl.counter);
   DeviceInfo dev;
   if (ra_status st = current_device(&dev)) return st;
   const int grid = static_cast<int>(n_items < dev.num_sms ? n_items : dev.num_sms);
-  cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(int32_t), s);
-  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
   return head_dim == 128 ? launch_decode<128>(p, grid, smem, s) : launch_decode<64>(p, grid, smem, s);
 }

@@ -57,7 +57,9 @@ struct DecodePlan {
 };
 
 struct DecodeWorkspace {
-  size_t part_o = 0, part_lse = 0, casc_o = 0, casc_lse = 0, key_start = 0, counter = 0, total = 0;
+  size_t part_o = 0, part_lse = 0, casc_o = 0, casc_lse = 0;
+  size_t ints = 0, ints_bytes = 0;  // one zeroed block: key_start [batch], counter [1]
+  size_t total = 0;
 };
 
 constexpr int kMaxHeadsPerCta = 8;  // consumer warps of the decode kernel
@@ -73,8 +75,8 @@ struct CascadeArgs {
 
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seq_len,
                        int32_t num_groups, int32_t max_group_prefix_len, int32_t max_group_size);
-DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int32_t head_dim,
-                                        const DecodePlan& pl, bool cascade);
+DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, const DecodePlan& pl, bool cascade);
 
 // Tensor-core pass over each group's shared prefix: writes p.casc_o / p.casc_lse
 // for every member (defined with the tcgen05 attention kernel).

@@ -134,6 +134,7 @@ ra_status launch_cascade_prefix(const DecodeParams& d, const CascadeArgs& ca, in
   p.max_csplits = d.max_csplits;
   p.casc_o = d.casc_o;
   p.casc_lse = d.casc_lse;
+  p.key_start = const_cast<int32_t*>(d.key_start);
   const int members_per_cta = tc::kTiles * (128 / d.group);
   const int mtiles = (ca.max_group_size + members_per_cta - 1) / members_per_cta;
   const int grid_x = mtiles * d.max_csplits;
