@@ -87,10 +87,13 @@ namespace tc {
 constexpr int kRows = 128;     // query rows per tile (MMA M)
 constexpr int kTiles = 2;      // query tiles per CTA
 constexpr int kKeys = 128;     // keys per tile (MMA N of S, K of PV)
-constexpr int kThreads = 352;  // 11 warps
-constexpr int kKWarp = 8;
-constexpr int kVWarp = 9;
-constexpr int kMmaWarp = 10;
+constexpr int kKWarps = 4;                 // TMA gather throughput grows with the number of issuing warps;
+constexpr int kVWarps = 3;                 // the tensor core waits on K first, so K gets one warp more
+constexpr int kKWarp0 = 8;                 // K gather warps 8..11
+constexpr int kVWarp0 = kKWarp0 + kKWarps;  // V gather warps 12..14
+constexpr int kMmaWarp = kVWarp0 + kVWarps;  // warp 15
+constexpr int kThreads = 32 * (kMmaWarp + 1);  // 512
+constexpr int kGroups = kKeys / 4;          // 4-key gather groups per tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -213,13 +216,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 
   if (threadIdx.x == 0) {
     s_abort = 0;
-    mbar_init(smem_u32(&bar_q), 1);
+    mbar_init(smem_u32(&bar_q), EXTEND ? 1 : kKWarps);
     for (int s = 0; s < KS; ++s) {
-      mbar_init(smem_u32(&bar_kf[s]), 1);
+      mbar_init(smem_u32(&bar_kf[s]), kKWarps);
       mbar_init(smem_u32(&bar_ke[s]), 1);
     }
     for (int s = 0; s < VS; ++s) {
-      mbar_init(smem_u32(&bar_vf[s]), 1);
+      mbar_init(smem_u32(&bar_vf[s]), kVWarps);
       mbar_init(smem_u32(&bar_ve[s]), 1);
     }
     for (int i = 0; i < kTiles; ++i) {
@@ -244,16 +247,18 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     flag_error(p.err, RA_DEVERR_TIMEOUT);
   };
 
-  if (warp == kKWarp || warp == kVWarp) {
+  if (warp >= kKWarp0 && warp < kMmaWarp) {
     // ================================================================ producers (TMA)
-    const bool is_v = warp == kVWarp;
+    const bool is_v = warp >= kVWarp0;
+    const int nw = is_v ? kVWarps : kKWarps;
+    const int pw = warp - (is_v ? kVWarp0 : kKWarp0);  // 0 .. nw-1
     const CUtensorMap* map = is_v ? &vmap : &kmap;
     if (lane == 0) prefetch_tensormap(map);
-    // ---- query tiles (K warp)
-    if (warp == kKWarp) {
+    // ---- query tiles (K warps)
+    if (!is_v) {
       const uint32_t bq = smem_u32(&bar_q);
       if constexpr (EXTEND) {
-        if (lane == 0) {
+        if (pw == 0 && lane == 0) {
           prefetch_tensormap(&qmap);
           mbar_arrive_expect_tx(bq, kTiles * kRows * D * 2);
 #pragma unroll
@@ -269,10 +274,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
           }
         }
       } else {
-        // the members' decode query rows, gathered 4 rows per TMA: CTA row R = (member R / G, q head kh*G + R % G)
-        if (lane == 0) mbar_arrive_expect_tx(bq, kTiles * kRows * D * 2);
+        // the members' decode query rows, 4 rows per TMA gather: CTA row R = (member R / G, q head kh*G + R % G);
+        // each K warp gathers a quarter of the 256 rows (16 groups of 4)
+        constexpr int kQGroups = kTiles * kRows / 4 / kKWarps;
+        if (lane == 0) mbar_arrive_expect_tx(bq, kQGroups * 4 * D * 2);
         __syncwarp();
-        for (int grp = lane; grp < kTiles * kRows / 4; grp += 32) {
+        if (lane < kQGroups) {
+          const int grp = pw * kQGroups + lane;
           int32_t qrow[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -290,44 +298,55 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         }
       }
     }
-    // ---- K (warp 8) or V (warp 9) tiles: lane l gathers keys 4l .. 4l+3 of each 128-key tile.
-    // The slot ids of tile j+1 are loaded while tile j is issued (their latency leaves the issue path).
+    // ---- K or V tiles: warp pw of nw gathers 4-key groups g0 .. g1-1 of each 128-key tile (keys 4*g0 ..),
+    // lane i < g1-g0 issuing the gather4 of group g0+i.  Slot ids: lane l holds keys 4*g0 + l and 4*g0 + 32 + l.
+    // The slot ids of tile j+1 are loaded while tile j is issued.
+    const int g0 = pw * kGroups / nw, g1 = (pw + 1) * kGroups / nw;
+    const int nkeys = 4 * (g1 - g0);  // <= 44
     uint64_t* full = is_v ? bar_vf : bar_kf;
     uint64_t* empty = is_v ? bar_ve : bar_ke;
     const int ns = is_v ? VS : KS;
-    auto load_rows = [&](int j, int32_t (&rowc)[4]) {  // tensor-map row of each key: slot * Hkv + kh
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int32_t key = kbeg + j * kKeys + lane * 4 + e;  // keys past the range repeat the last key
-        int32_t s = __ldg(row_ptr + min(key, kend - 1));
-        if (s < 0 || s >= p.num_slots) {
-          flag_error(p.err, RA_DEVERR_SLOT);
-          s = 0;
-        }
-        rowc[e] = s * p.hkv + kh;
+    auto load_row = [&](int j, int k) -> int32_t {  // tensor-map row (slot * Hkv + kh) of key 4*g0 + k
+      if (k >= nkeys) return 0;
+      const int32_t key = kbeg + j * kKeys + 4 * g0 + k;  // keys past the range repeat the last key
+      int32_t s = __ldg(row_ptr + min(key, kend - 1));
+      if (s < 0 || s >= p.num_slots) {
+        flag_error(p.err, RA_DEVERR_SLOT);
+        s = 0;
       }
+      return s * p.hkv + kh;
     };
     int issued = 0;
-    int32_t cur[4], nxt[4];
-    load_rows(0, cur);
+    int32_t ca = load_row(0, lane), cb = load_row(0, lane + 32);
     for (int j = 0; j < nt; ++j) {
       if (aborted(abort_flag)) break;
       const int st = j % ns;
-      if (j + 1 < nt) load_rows(j + 1, nxt);
+      const int32_t na = j + 1 < nt ? load_row(j + 1, lane) : 0;
+      const int32_t nb = j + 1 < nt ? load_row(j + 1, lane + 32) : 0;
       if (j >= ns && !mbar_wait(smem_u32(&empty[st]), ((j / ns) + 1) & 1)) {
         give_up();
         break;
       }
       const uint32_t tile = is_v ? sV(st) : sK(st);
-      if (lane == 0) mbar_arrive_expect_tx(smem_u32(&full[st]), kKeys * D * 2);
+      int32_t r[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int k = lane * 4 + e;  // key of this lane's group (meaningful for lane < g1-g0)
+        const int32_t va = __shfl_sync(0xffffffffu, ca, k & 31);
+        const int32_t vb = __shfl_sync(0xffffffffu, cb, k & 31);
+        r[e] = k < 32 ? va : vb;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(smem_u32(&full[st]), nkeys * D * 2);
       __syncwarp();
+      if (lane < g1 - g0) {
+        const int row = 4 * (g0 + lane);  // first tile row of this gather
 #pragma unroll
-      for (int h = 0; h < HALVES; ++h)
-        tma_gather4(tile + h * (kRows * 128) + lane * 4 * 128, map, h * 64, cur[0], cur[1], cur[2], cur[3],
-                    smem_u32(&full[st]));
+        for (int h = 0; h < HALVES; ++h)
+          tma_gather4(tile + h * (kRows * 128) + row * 128, map, h * 64, r[0], r[1], r[2], r[3], smem_u32(&full[st]));
+      }
       issued = j + 1;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) cur[e] = nxt[e];
+      ca = na;
+      cb = nb;
     }
     // copies this warp issued land before the CTA can leave (normally consumed already)
     for (int j = (issued > ns ? issued - ns : 0); j < issued; ++j)
@@ -407,27 +426,34 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       const bool fail_here = aborted(abort_flag) || !mbar_wait(smem_u32(&bar_s[ti]), j & 1);
       if (__any_sync(0xffffffffu, fail_here)) { ok = false; break; }  // warp-uniform: tcgen05.ld/st are collective
       tc_fence_after();
-      uint32_t sr[kKeys];
-#pragma unroll
-      for (int c = 0; c < kKeys / 32; ++c) {
-        uint32_t (&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]);
-        tmem_ld32(tmem + lane_addr + col_s + c * 32, chunk);
-      }
-      tc_wait_ld();
       const int32_t key0 = kbeg + j * kKeys;
-      // row max of the raw scores (scale > 0 commutes with max), 8 independent chains
+      const bool masked = key0 + kKeys > lim;
+      // pass 1: row max of the raw scores (scale > 0 commutes with max), 8 independent chains; the next
+      // 32-column TMEM load is in flight while the current chunk is reduced
       float mx8[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-      if (key0 + kKeys > lim) {
+      auto max_chunk = [&](const uint32_t (&sr)[32], int c) {
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) {
-          if (key0 + c >= lim) sr[c] = __float_as_uint(-INFINITY);
-          mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sr[c]));
+        for (int e = 0; e < 32; ++e) {
+          const float x = (masked && key0 + c * 32 + e >= lim) ? -INFINITY : __uint_as_float(sr[e]);
+          mx8[e & 7] = fmaxf(mx8[e & 7], x);
         }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kKeys; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], __uint_as_float(sr[c]));
+      };
+      {
+        uint32_t ba[32], bb[32];
+        tmem_ld32(tmem + lane_addr + col_s, ba);
+        tc_wait_ld_regs(ba);
+        tmem_ld32(tmem + lane_addr + col_s + 32, bb);
+        max_chunk(ba, 0);
+        tc_wait_ld_regs(bb);
+        tmem_ld32(tmem + lane_addr + col_s + 64, ba);
+        max_chunk(bb, 1);
+        tc_wait_ld_regs(ba);
+        tmem_ld32(tmem + lane_addr + col_s + 96, bb);
+        max_chunk(ba, 2);
+        tc_wait_ld_regs(bb);
+        max_chunk(bb, 3);
       }
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.scale_log2;
@@ -436,23 +462,46 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       const float m_ref = resc ? m_new : m_used;
       const float m_sub = (m_ref == -INFINITY) ? 0.f : m_ref;
       const float alpha = resc ? ex2(m_used - m_sub) : 1.f;
-      // p = 2^(s * scale_log2 - m_ref): one FMA + one MUFU per score; 8 independent partial sums
-      float sum8[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sum8[e] = 0.f;
-#pragma unroll
-      for (int c = 0; c < kKeys / 32; ++c) {
+      // pass 2: p = 2^(s * scale_log2 - m_ref): packed FMA pairs + one MUFU per score, packed to bf16 over S
+      const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
+      const uint64_t neg_m2 = f2_pack(-m_sub, -m_sub);
+      uint64_t sum2[4] = {0, 0, 0, 0};  // 4 independent chains of (even, odd) partial sums
+      auto exp_chunk = [&](const uint32_t (&sr)[32], int c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[c * 32 + 2 * e]), p.scale_log2, -m_sub));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[c * 32 + 2 * e + 1]), p.scale_log2, -m_sub));
-          sum8[(2 * e) & 7] += p0;
-          sum8[(2 * e + 1) & 7] += p1;
+          float s0 = __uint_as_float(sr[2 * e]), s1 = __uint_as_float(sr[2 * e + 1]);
+          if (masked) {
+            if (key0 + c * 32 + 2 * e >= lim) s0 = -INFINITY;
+            if (key0 + c * 32 + 2 * e + 1 >= lim) s1 = -INFINITY;
+          }
+          float t0, t1;
+          f2_unpack(f2_fma(f2_pack(s0, s1), scale2, neg_m2), t0, t1);
+          const float p0 = ex2(t0), p1 = ex2(t1);
+          sum2[e & 3] = f2_add(sum2[e & 3], f2_pack(p0, p1));
           pk[e] = pack_bf16x2(p0, p1);
         }
+        // P columns 16c .. 16c+15 overwrite S columns already read
         tmem_st16(tmem + lane_addr + col_s + c * 16, pk);
+      };
+      {
+        uint32_t ba[32], bb[32];
+        tmem_ld32(tmem + lane_addr + col_s, ba);
+        tc_wait_ld_regs(ba);
+        tmem_ld32(tmem + lane_addr + col_s + 32, bb);
+        exp_chunk(ba, 0);  // writes P columns 0..15: S chunk 0, already in registers
+        tc_wait_ld_regs(bb);
+        tmem_ld32(tmem + lane_addr + col_s + 64, ba);
+        exp_chunk(bb, 1);  // P columns 16..31
+        tc_wait_ld_regs(ba);
+        tmem_ld32(tmem + lane_addr + col_s + 96, bb);
+        exp_chunk(ba, 2);  // P columns 32..47: S chunk 1, already read
+        tc_wait_ld_regs(bb);
+        exp_chunk(bb, 3);  // P columns 48..63
       }
+      float sum8[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) f2_unpack(sum2[e], sum8[2 * e], sum8[2 * e + 1]);
       const float rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       l = l * alpha + rowsum;
       if (j > 0) {
@@ -466,7 +515,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
           for (int c = 0; c < D / 32; ++c) {
             uint32_t ov[32];
             tmem_ld32(tmem + lane_addr + col_o + c * 32, ov);
-            tc_wait_ld();
+            tc_wait_ld_regs(ov);
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
             tmem_st32(tmem + lane_addr + col_o + c * 32, ov);
@@ -490,7 +539,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
           tmem_ld32(tmem + lane_addr + col_o + c * 32, ov);
-          tc_wait_ld();
+          tc_wait_ld_regs(ov);
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
@@ -510,7 +559,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
           tmem_ld32(tmem + lane_addr + col_o + c * 32, ov);
-          tc_wait_ld();
+          tc_wait_ld_regs(ov);
           if (write) {
             float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
 #pragma unroll
