@@ -7,6 +7,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <utility>
 
 #include "../../include/ra.h"
 
@@ -32,6 +33,28 @@ ra_status current_device(DeviceInfo* out);
 
 // Map the last launch error (if any) to RA_ERR_CUDA with a message.
 ra_status check_launch(const char* what);
+
+// Launch `kern` on `stream` with programmatic stream serialization: it may start while the previous
+// kernel on the stream runs, once every CTA of that kernel has called griddepcontrol.launch_dependents.
+// Every kernel of this library calls griddepcontrol.wait before it touches memory its predecessor may
+// still be writing or reading, so the early start only overlaps launch latency, prologues and tails.
+template <typename... KArgs, typename... Args>
+ra_status launch_pdl(const char* what, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(e));
+  return RA_OK;
+}
 
 }  // namespace ra
 

@@ -79,7 +79,6 @@ struct TcParams {
   int32_t max_csplits;
   float* casc_o;
   float* casc_lse;
-  int32_t* key_start;  // [batch]: the prefix pass records each member's group prefix length here
 };
 
 namespace tc {
@@ -133,6 +132,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
+  griddep_wait();  // the previous kernel (e.g. the KV store of this step) has completed
+  griddep_launch();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.group;
@@ -197,12 +198,6 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     if (table_row < 0 || table_row >= p.table_rows) {
       if (blockIdx.x == 0 && kh == 0 && threadIdx.x == 0) flag_error(p.err, RA_DEVERR_TABLE);
       return;
-    }
-    // members read only their own positions Pg .. L-1 in the private decode
-    if (csplit == 0 && kh == 0 && static_cast<int>(threadIdx.x) < n_valid) {
-      const int32_t b = __ldg(p.group_reqs + mem0 + threadIdx.x);
-      if (b >= 0 && b < p.batch) p.key_start[b] = Pg;
-      else flag_error(p.err, RA_DEVERR_TABLE);
     }
   }
   const int32_t nt = (kend - kbeg + kKeys - 1) / kKeys;  // >= 1

@@ -101,6 +101,10 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + 1), 1) decode_kernel(c
   int32_t* s_slots = reinterpret_cast<int32_t*>(smem + 256);
   const uint32_t stage0 = sbase + kHdrBytes;
   const int RS = p.row_stride;
+  // Let the combine launch; this kernel reads nothing its predecessor (the cascade prefix pass, which
+  // only writes prefix partials) produces, so it does not wait for it here.  It waits before leaving,
+  // so that its completion implies the prefix pass's (the combine reads both).
+  griddep_launch();
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -195,9 +199,13 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + 1), 1) decode_kernel(c
       // copies this warp issued must land before the CTA leaves
       for (int32_t j = (c > ns ? c - ns : 0); j < c; ++j) mbar_wait(full0 + 8 * (j % ns), (j / ns) & 1);
     }
+    griddep_wait();
     return;
   }
-  if (warp > nc) return;
+  if (warp > nc) {
+    griddep_wait();
+    return;
+  }
 
   // ================================================================ consumers
   const int g = lane >> 2;  // q head within the GQA group (MMA N index)
@@ -339,6 +347,7 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + 1), 1) decode_kernel(c
     *s_abort = 1;
     flag_error(p.err, RA_DEVERR_TIMEOUT);
   }
+  griddep_wait();
 }
 
 // Merge the partials of every request that has more than one (the shared-prefix pass's and the
@@ -348,6 +357,8 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + 1), 1) decode_kernel(c
 template <int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
   constexpr int V = D / 32;
+  griddep_wait();  // the decode kernel (and, through it, the prefix pass) has completed
+  griddep_launch();
   const int warp_global = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (warp_global >= p.batch * p.hq) return;
@@ -398,6 +409,28 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
         __floats2bfloat162_rn(acc[v] * inv, acc[v + 1] * inv);
 }
 
+// key_start[b] = prefix length of b's cascade group (0 for requests in no group, set by the memset).
+__global__ void cascade_key_start_kernel(int32_t* key_start, int32_t batch, const int32_t* group_indptr,
+                                         const int32_t* group_reqs, const int32_t* group_prefix_len,
+                                         int32_t num_groups, uint32_t* err) {
+  griddep_wait();
+  griddep_launch();
+  const int32_t total = __ldg(group_indptr + num_groups);
+  for (int32_t m = blockIdx.x * blockDim.x + threadIdx.x; m < total; m += gridDim.x * blockDim.x) {
+    int32_t lo = 0, hi = num_groups;  // group g with indptr[g] <= m < indptr[g+1]
+    while (hi - lo > 1) {
+      const int32_t mid = (lo + hi) >> 1;
+      if (__ldg(group_indptr + mid) <= m) lo = mid; else hi = mid;
+    }
+    const int32_t b = __ldg(group_reqs + m);
+    if (b < 0 || b >= batch) {
+      flag_error(err, RA_DEVERR_TABLE);
+      continue;
+    }
+    key_start[b] = __ldg(group_prefix_len + lo);
+  }
+}
+
 template <int D>
 ra_status launch_decode(const DecodeParams& p, int grid, int smem, cudaStream_t stream) {
   auto kern = decode_kernel<D>;
@@ -410,11 +443,9 @@ ra_status launch_decode(const DecodeParams& p, int grid, int smem, cudaStream_t 
     if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaFuncSetAttribute(decode): %s", cudaGetErrorString(e));
     configured[dev.device] = kSmemLimit;
   }
-  kern<<<grid, 32 * (p.hpc + 1), smem, stream>>>(p);
-  if (ra_status st = check_launch("decode_kernel")) return st;
+  if (ra_status st = launch_pdl("decode_kernel", kern, dim3(grid), dim3(32 * (p.hpc + 1)), smem, stream, p)) return st;
   const int nwarps = p.batch * p.hq;
-  decode_combine_kernel<D><<<(nwarps + 3) / 4, 128, 0, stream>>>(p);
-  return check_launch("decode_combine_kernel");
+  return launch_pdl("decode_combine_kernel", decode_combine_kernel<D>, dim3((nwarps + 3) / 4), dim3(128), 0, stream, p);
 }
 
 }  // namespace
@@ -428,8 +459,9 @@ static int32_t heads_per_cta(int32_t num_kv_heads) {
 
 // Private keys per work item: between 256 and 1024, aiming at ~1K (request, split, head group)
 // items over the host-side bound of the batch's keys.
-// Shared-prefix pass (cascade): 128-row tiles of (member, q head) per group and kv head; the prefix is
-// split in multiples of 128 keys until there are about two CTAs per SM of work.
+// Shared-prefix pass (cascade): 256-row tiles of (member, q head) per group and kv head; the prefix is
+// split in multiples of 128 keys until there are about 96 CTAs, under one wave, so the persistent private
+// decode (launched programmatically after it) runs on the remaining SMs at the same time.
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seq_len,
                        int32_t num_groups, int32_t max_group_prefix_len, int32_t max_group_size) {
   DecodePlan pl;
@@ -448,7 +480,7 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
     const int64_t mtiles = (max_group_size + members_per_cta - 1) / members_per_cta;
     const int64_t base = static_cast<int64_t>(num_groups) * num_kv_heads * mtiles;
     const int64_t key_tiles = (max_group_prefix_len + 127) / 128;
-    int64_t want = (304 + base - 1) / base;
+    int64_t want = (96 + base - 1) / base;  // about 96 CTAs: the rest of the SMs start the private decode meanwhile
     if (want < 1) want = 1;
     if (want > key_tiles) want = key_tiles;
     const int64_t tiles_per_split = (key_tiles + want - 1) / want;
@@ -572,7 +604,11 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
     p.max_csplits = pl.max_csplits;
     p.casc_o = reinterpret_cast<float*>(ws + wl.casc_o);
     p.casc_lse = reinterpret_cast<float*>(ws + wl.casc_lse);
-    p.key_start = ints;  // written by the prefix pass for every member (0 for other requests)
+    p.key_start = ints;
+    if (ra_status st = launch_pdl("cascade_key_start_kernel", cascade_key_start_kernel, dim3((batch + 127) / 128),
+                                  dim3(128), 0, s, ints, batch, group_indptr, group_reqs, group_prefix_len, num_groups,
+                                  device_error))
+      return st;
     CascadeArgs ca{group_indptr, group_reqs, group_prefix_len, num_groups, max_group_prefix_len, max_group_size};
     if (ra_status st = launch_cascade_prefix(p, ca, head_dim, s)) return st;
   }

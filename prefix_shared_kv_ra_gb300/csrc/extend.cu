@@ -82,8 +82,7 @@ ra_status launch_extend(const TcParams& p, const CUtensorMap& qmap, int max_tile
     return fail(RA_ERR_UNSUPPORTED, "extend kernel needs %d bytes of shared memory", L::kDynSmem);
   if (ra_status st = set_smem(kern, L::kDynSmem, configured, dev.device)) return st;
   dim3 grid(max_tiles, p.hkv, batch);
-  kern<<<grid, tc::kThreads, L::kDynSmem, s>>>(p, qmap, kmap, vmap);
-  return check_launch("attn_tc_kernel<extend>");
+  return launch_pdl("attn_tc_kernel<extend>", kern, grid, dim3(tc::kThreads), L::kDynSmem, s, p, qmap, kmap, vmap);
 }
 
 template <int D>
@@ -101,8 +100,8 @@ ra_status launch_prefix(const TcParams& p, int grid_x, int num_groups, cudaStrea
   if (ra_status st = row_gather_map(&kmap, p.k_pool, p.num_slots * p.hkv, D)) return st;
   if (ra_status st = row_gather_map(&vmap, p.v_pool, p.num_slots * p.hkv, D)) return st;
   dim3 grid(grid_x, p.hkv, num_groups);
-  kern<<<grid, tc::kThreads, L::kDynSmem, s>>>(p, qmap, kmap, vmap);
-  return check_launch("attn_tc_kernel<cascade prefix>");
+  return launch_pdl("attn_tc_kernel<cascade prefix>", kern, grid, dim3(tc::kThreads), L::kDynSmem, s, p, qmap, kmap,
+                    vmap);
 }
 
 }  // namespace
@@ -134,7 +133,6 @@ ra_status launch_cascade_prefix(const DecodeParams& d, const CascadeArgs& ca, in
   p.max_csplits = d.max_csplits;
   p.casc_o = d.casc_o;
   p.casc_lse = d.casc_lse;
-  p.key_start = const_cast<int32_t*>(d.key_start);
   const int members_per_cta = tc::kTiles * (128 / d.group);
   const int mtiles = (ca.max_group_size + members_per_cta - 1) / members_per_cta;
   const int grid_x = mtiles * d.max_csplits;

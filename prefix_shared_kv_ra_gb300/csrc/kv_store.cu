@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(256) kv_store_kernel(uint4* __restrict__ k_poo
                                                        const uint4* __restrict__ v_new,
                                                        const int32_t* __restrict__ loc, int64_t total_vecs,
                                                        uint32_t* __restrict__ err) {
+  griddep_wait();  // earlier kernels may still read the pool rows this store overwrites
+  griddep_launch();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_vecs; i += stride) {
     const int64_t tok = i / row_vecs;
@@ -65,8 +67,8 @@ extern "C" ra_status ra_kv_store(void* k_pool, void* v_pool, int64_t num_slots, 
   const int64_t want = (total + threads - 1) / threads;
   const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
   const int blocks = static_cast<int>(want < cap ? want : cap);
-  kv_store_kernel<<<blocks, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), num_slots, row_vecs,
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), out_cache_loc, total, device_error);
-  return check_launch("kv_store_kernel");
+  return launch_pdl("kv_store_kernel", kv_store_kernel, dim3(blocks), dim3(threads), 0,
+                    reinterpret_cast<cudaStream_t>(stream), static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool),
+                    num_slots, row_vecs, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
+                    out_cache_loc, total, device_error);
 }

@@ -64,6 +64,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return true;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Wait until the grid this one was launched after (with programmatic stream serialization) has
+// completed and its memory is visible; a no-op for a normally launched grid.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next grid on the stream (if launched with programmatic serialization) to start launching.
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- bulk copies
 // 1-D bulk copy global -> shared (this CTA), completion counted in bytes on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
