@@ -36,7 +36,7 @@ METRIC = "attn tokens/s; decode KV GB/s and extend TFLOP/s as % of GB300 rooflin
 UNIT = "tokens/s"
 WORKLOAD = ("multi-turn chat mix, 70B heads (64 q / 8 kv, head_dim 128, bf16): 256 requests, lognormal "
             "contexts (median 2048, clipped 16..32768), radix-tree prefix sharing at 70% token hit ratio; "
-            "32 extend (suffix 64..512) + 224 decode; pool 2M slots")
+            "32 extend (suffix 64..512) + 224 decode (cascade groups from the radix tree); pool 2M slots")
 L2_FLUSH_BYTES = 256 << 20
 KV_BYTES_PER_TOKEN_HEAD = 2 * 128 * 2  # K + V row of one kv head, bf16
 
@@ -76,6 +76,37 @@ def decode_bytes(b, cascade: bool = False) -> dict:
 
 def store_bytes(b) -> int:
     return 2 * 2 * b.num_new_tokens * b.num_kv_heads * b.head_dim * 2  # read + write, K and V
+
+
+# ----------------------------------------------------------------------------- ncu traffic
+def source_digest() -> str:
+    """Digest of the CUDA sources and the C header: ties a recorded ncu traffic figure to the code."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "prefix_shared_kv_ra_gb300", "csrc", "*"))) + \
+        [os.path.join(ROOT, "include", "ra.h")]
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from profiles/ncu_traffic.md (lines 'traffic: kernel=.. workload=.. bytes=..
+    source=..'), or None when absent or taken on other sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+    if not os.path.exists(path):
+        return None
+    digest = source_digest()
+    for line in open(path):
+        line = line.strip().strip("`")
+        if not line.startswith("traffic:"):
+            continue
+        kv = dict(x.split("=", 1) for x in line[len("traffic:"):].split())
+        if kv.get("kernel") == kernel and kv.get("workload") == workload and kv.get("source") == digest:
+            return float(kv["bytes"])
+    return None
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -134,6 +165,14 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def with_tree_groups(b, min_prefix: int = 256):
+    """Attach the cascade groups the radix tree derives from the batch's decode table rows."""
+    from prefix_shared_kv_ra_gb300.radix import cascade_groups
+    rows = [b.req_to_token[r, :L] for r, L in zip(b.dec_rpi, b.dec_seq_lens)]
+    b.casc_group_indptr, b.casc_group_reqs, b.casc_group_prefix_len = cascade_groups(rows, min_prefix=min_prefix)
+    return b
+
+
 # ----------------------------------------------------------------------------- GPU arm
 class Step:
     """The hot path on one batch, resident on the device."""
@@ -177,6 +216,7 @@ class Step:
                                            self.casc.get("max_group_size", 0))
         self.ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
         # kernel launches per step (the library's launch structure)
+        # kernel launches per step: store, extend, [key_start scatter, prefix pass,] decode, combine
         self.launches = 1 + (1 if b.n_extend else 0) + ((2 + (2 if self.cascade else 0)) if b.n_decode else 0)
 
     def run(self, d=None, events=None):
@@ -202,13 +242,16 @@ class Step:
             ev[3].record()
 
 
-def time_steps(step, steps: int, warmup: int, flush, sample_clocks_uuid=None):
+def time_steps(step, steps: int, warmup: int, flush, sample_clocks_uuid=None, breakdown: bool = True):
+    """Headline pass: events around each whole step only (the kernels of a step may overlap through
+    programmatic dependent launch).  Breakdown pass: events between the three calls as well (which
+    serialises them) for the per-kernel times the roofline uses."""
     torch = step.torch
     for _ in range(warmup):
         flush.zero_()
         step.run()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     sampler = ClockSampler(sample_clocks_uuid) if sample_clocks_uuid is not None else None
     if sampler:
         sampler.__enter__()
@@ -217,17 +260,24 @@ def time_steps(step, steps: int, warmup: int, flush, sample_clocks_uuid=None):
         t0 = time.perf_counter()
         for k in range(steps):
             flush.zero_()
-            step.run(events=evs[k])
+            step.run(events=[evs[k][0], None, None, evs[k][1]])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     finally:
         if sampler:
             sampler.__exit__(None, None, None)
-    per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evs])  # ms: store, extend, decode
-    total = np.array([e[0].elapsed_time(e[3]) for e in evs])
-    err = int(step.err.item())
-    return {"store_ms": per[:, 0], "extend_ms": per[:, 1], "decode_ms": per[:, 2], "step_ms": total,
-            "wall_s": wall, "clocks": sampler.summary() if sampler else None, "device_error": err}
+    total = np.array([e[0].elapsed_time(e[1]) for e in evs])
+    out = {"step_ms": total, "wall_s": wall, "clocks": sampler.summary() if sampler else None}
+    if breakdown:
+        evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        for k in range(steps):
+            flush.zero_()
+            step.run(events=evb[k])
+        torch.cuda.synchronize()
+        per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evb])  # store, extend, decode
+        out.update(store_ms=per[:, 0], extend_ms=per[:, 1], decode_ms=per[:, 2])
+    out["device_error"] = int(step.err.item())
+    return out
 
 
 def e2e_steps(step, steps: int, warmup: int, flush):
@@ -326,7 +376,9 @@ def oracle_sample(b, budget_s: float, seed: int = 0):
         v = (ext_keys[se].sum() if se is not None else 0) + (dec_keys[sd].sum() if sd is not None else 0)
         return time.perf_counter() - t0, float(v)
 
-    # calibrate on a small sample, then time one sample sized to about budget_s
+    # calibrate on small samples (the first also pays one-time start-up), then time one sample sized to
+    # about budget_s
+    timed(16, 16)
     dt, v = timed(64, 64)
     scale = max(1.0, budget_s / max(dt, 1e-3))
     n_e = int(min(ext_keys.size, 64 * scale))
@@ -360,6 +412,7 @@ def run_reference(args):
 # ----------------------------------------------------------------------------- ncu cases
 PROFILE_CASES = {
     "extend_fewshot": ("cfg3_fewshot_extend", False),
+    "multiturn_mix_cascade": ("cfg5_multiturn_mix_70b", True),
     "decode_8b": ("cfg2_decode_8b", False),
     "decode_8b_cascade": ("cfg2_decode_8b", True),
     "decode_70b_forked_cascade": ("cfg4_forked_decode_70b", True),
@@ -375,7 +428,10 @@ def run_profile_case(name: str, steps: int):
     ra.load()
     cfg, cascade = PROFILE_CASES[name]
     dev = torch.device("cuda:0")
-    st = Step(W.CONFIGS[cfg](), dev, cascade=cascade)
+    b = W.CONFIGS[cfg]()
+    if cascade and not b.has_cascade():
+        b = with_tree_groups(b)
+    st = Step(b, dev, cascade=cascade)
     for _ in range(steps):
         st.run()
     torch.cuda.synchronize()
@@ -425,9 +481,10 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     peaks = load_peaks()
 
-    # independent replicas: each rank draws its own batch of the same workload
-    b = W.cfg5_multiturn_mix_70b(seed=5 + rank)
-    step = Step(b, dev)
+    # independent replicas: each rank draws its own batch of the same workload; the decode requests are
+    # grouped by the radix tree (one-level cascade groups over shared prefixes of >= 256 tokens)
+    b = with_tree_groups(W.cfg5_multiturn_mix_70b(seed=5 + rank))
+    step = Step(b, dev, cascade=True)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     uuid = None
     try:
@@ -469,12 +526,14 @@ def main():
     if ext_ms >= dec_ms:
         roof = {"kernel": "attn_tc_kernel<extend>", "bound": "tensor", "achieved": ext_tf,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ext_tf / peaks["bf16_tflops"],
-                "traffic": None, "peak_source": peaks["source"] + " bf16 burst",
+                "traffic": recorded_traffic("attn_tc_kernel<extend>", "multiturn_mix"),
+                "peak_source": peaks["source"] + " bf16 burst",
                 "per_launch": {"flops": fl, "ms": ext_ms}}
     else:
-        roof = {"kernel": "decode_split_kernel + decode_combine_kernel", "bound": "hbm", "achieved": dec_gbs,
+        roof = {"kernel": "decode_kernel + decode_combine_kernel", "bound": "hbm", "achieved": dec_gbs,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
-                "traffic": None, "peak_source": peaks["source"] + " HBM copy",
+                "traffic": recorded_traffic("decode_kernel", "multiturn_mix"),
+                "peak_source": peaks["source"] + " HBM copy",
                 "per_launch": {"bytes": dbytes["algorithmic"], "ms": dec_ms}}
     extra = {} if args.no_extra else extra_kernels(dev, flush, peaks)
     cpu = oracle_sample(b, args.cpu_budget)
@@ -501,6 +560,7 @@ def main():
         "e2e": {"value": tokens * world / e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches * args.steps,
+        "source_digest": source_digest(),
         "clocks": r["clocks"],
         "device_error": r["device_error"],
         "peaks": peaks,

@@ -124,7 +124,6 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
                    const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
   using namespace tc;
   using L = Layout<D, KS, VS>;
-  constexpr int NSMAX = KS > VS ? KS : VS;
   constexpr int HALVES = D / 64;  // 128-byte (64-element) column blocks of a row
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_q, bar_kf[KS], bar_ke[KS], bar_vf[VS], bar_ve[VS], bar_s[kTiles],

@@ -459,9 +459,9 @@ static int32_t heads_per_cta(int32_t num_kv_heads) {
 
 // Private keys per work item: between 256 and 1024, aiming at ~1K (request, split, head group)
 // items over the host-side bound of the batch's keys.
-// Shared-prefix pass (cascade): 256-row tiles of (member, q head) per group and kv head; the prefix is
-// split in multiples of 128 keys until there are about 96 CTAs, under one wave, so the persistent private
-// decode (launched programmatically after it) runs on the remaining SMs at the same time.
+// Shared-prefix pass (cascade): 256-row tiles of (member, q head) per group and kv head; each CTA covers
+// at most `cchunk` prefix keys (about 96 CTAs, at most 2048 keys each).  The persistent private decode is
+// launched programmatically after it and runs on the SMs the prefix pass leaves free.
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seq_len,
                        int32_t num_groups, int32_t max_group_prefix_len, int32_t max_group_size) {
   DecodePlan pl;
@@ -475,17 +475,18 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
   pl.max_splits = static_cast<int32_t>((static_cast<int64_t>(max_seq_len) + chunk - 1) / chunk);
   if (pl.max_splits < 1) pl.max_splits = 1;
   if (num_groups > 0 && max_group_prefix_len > 0) {
+    // prefix keys per prefix-pass CTA: split so that about 96 CTAs exist (the rest of the SMs run the
+    // private decode meanwhile), but no CTA covers more than 2048 prefix keys; a multiple of the 128-key tile
     const int32_t group = num_q_heads / num_kv_heads;
-    const int32_t members_per_cta = 2 * (128 / (group > 0 ? group : 1));  // two 128-row query tiles
+    const int64_t members_per_cta = 2 * (128 / (group > 0 ? group : 1));  // two 128-row query tiles
     const int64_t mtiles = (max_group_size + members_per_cta - 1) / members_per_cta;
     const int64_t base = static_cast<int64_t>(num_groups) * num_kv_heads * mtiles;
-    const int64_t key_tiles = (max_group_prefix_len + 127) / 128;
-    int64_t want = (96 + base - 1) / base;  // about 96 CTAs: the rest of the SMs start the private decode meanwhile
-    if (want < 1) want = 1;
-    if (want > key_tiles) want = key_tiles;
-    const int64_t tiles_per_split = (key_tiles + want - 1) / want;
-    pl.cchunk = static_cast<int32_t>(tiles_per_split * 128);
-    pl.max_csplits = static_cast<int32_t>((max_group_prefix_len + pl.cchunk - 1) / pl.cchunk);
+    const int64_t want = (96 + base - 1) / base;
+    int64_t cchunk = (max_group_prefix_len + want - 1) / want;
+    cchunk = (cchunk + 127) / 128 * 128;
+    if (cchunk > 2048) cchunk = 2048;
+    pl.cchunk = static_cast<int32_t>(cchunk);
+    pl.max_csplits = static_cast<int32_t>((max_group_prefix_len + cchunk - 1) / cchunk);
   }
   return pl;
 }

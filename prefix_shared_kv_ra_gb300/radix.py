@@ -1,0 +1,237 @@
+"""Host-side radix-tree prefix cache over the token-granular KV pool.
+
+The cache maps token sequences to the pool slots that hold their K/V, so a
+new request reuses the slots of the longest cached prefix and only computes
+its suffix (SGLang paper summary, §3 "Efficient KV Cache Reuse with
+RadixAttention"; the yaopepe.com explainer, §04):
+
+* a node's edge is a run of tokens with the slots of those tokens;
+* matching walks from the root edge by edge; a match that ends inside an
+  edge splits it, so the shared part becomes a common ancestor (the
+  explainer's figure: S+A and S+B become S with children A and B);
+* running requests hold a reference on every node of their path; only
+  unreferenced leaves may be evicted, least recently used first, and a parent
+  that becomes an unreferenced leaf becomes a candidate in turn;
+* evicted slots go back to the slot pool for reuse.
+
+This is support code for the attention path: it produces the
+``req_to_token`` rows, the cascade groups and the hit ratio the kernels and
+the benchmarks use.  It holds no attention arithmetic.
+"""
+from __future__ import annotations
+
+import heapq
+import itertools
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+__all__ = ["SlotPool", "RadixCache", "cascade_groups"]
+
+
+class SlotPool:
+    """Free list of token slots [1, num_slots); slot 0 is the dummy slot padded requests write."""
+
+    def __init__(self, num_slots: int):
+        self.num_slots = int(num_slots)
+        self._free = list(range(self.num_slots - 1, 0, -1))  # pop() hands out low slots first
+
+    def available(self) -> int:
+        return len(self._free)
+
+    def alloc(self, n: int) -> Optional[np.ndarray]:
+        if n > len(self._free):
+            return None
+        out = [self._free.pop() for _ in range(n)]
+        return np.asarray(out, dtype=np.int32)
+
+    def free(self, slots: Sequence[int]) -> None:
+        for s in np.asarray(slots, dtype=np.int64).tolist():
+            if not 1 <= s < self.num_slots:
+                raise ValueError(f"slot {s} out of range")
+            self._free.append(int(s))
+
+
+class _Node:
+    __slots__ = ("key", "value", "children", "parent", "lock_ref", "last_access", "uid")
+    _ids = itertools.count()
+
+    def __init__(self, key: np.ndarray, value: np.ndarray, parent: Optional["_Node"]):
+        self.key = key          # int32 tokens of the edge into this node
+        self.value = value      # int32 slots of those tokens
+        self.children: Dict[int, "_Node"] = {}
+        self.parent = parent
+        self.lock_ref = 0
+        self.last_access = 0
+        self.uid = next(_Node._ids)
+
+
+def _common_len(a: np.ndarray, b: np.ndarray) -> int:
+    n = min(a.size, b.size)
+    if n == 0:
+        return 0
+    diff = np.nonzero(a[:n] != b[:n])[0]
+    return int(diff[0]) if diff.size else n
+
+
+class RadixCache:
+    def __init__(self, pool: SlotPool):
+        self.pool = pool
+        self.root = _Node(np.zeros(0, np.int32), np.zeros(0, np.int32), None)
+        self.root.lock_ref = 1  # never evicted
+        self._clock = 0
+
+    # ------------------------------------------------------------------ queries
+    def _tick(self) -> int:
+        self._clock += 1
+        return self._clock
+
+    def match_prefix(self, tokens: Sequence[int]) -> Tuple[np.ndarray, _Node]:
+        """Slots of the longest cached prefix of `tokens` and the node where it ends
+        (an edge matched part-way is split there)."""
+        key = np.asarray(tokens, dtype=np.int32)
+        node, pos, slots = self.root, 0, []
+        now = self._tick()
+        node.last_access = now
+        while pos < key.size:
+            child = node.children.get(int(key[pos]))
+            if child is None:
+                break
+            child.last_access = now
+            k = _common_len(child.key, key[pos:])
+            if k < child.key.size:
+                child = self._split(child, k)
+                slots.append(child.value)
+                node = child
+                pos += k
+                break
+            slots.append(child.value)
+            node = child
+            pos += k
+        value = np.concatenate(slots) if slots else np.zeros(0, np.int32)
+        return value.astype(np.int32), node
+
+    def _split(self, child: _Node, k: int) -> _Node:
+        """Make the first k tokens of child's edge a new node between child and its parent."""
+        parent = child.parent
+        mid = _Node(child.key[:k].copy(), child.value[:k].copy(), parent)
+        mid.lock_ref = child.lock_ref
+        mid.last_access = child.last_access
+        parent.children[int(mid.key[0])] = mid
+        child.key, child.value = child.key[k:].copy(), child.value[k:].copy()
+        child.parent = mid
+        mid.children[int(child.key[0])] = child
+        return mid
+
+    def insert(self, tokens: Sequence[int], slots: Sequence[int]) -> int:
+        """Insert tokens with their slots; returns how many leading tokens were already cached
+        (the caller frees its duplicate slots for those positions)."""
+        key = np.asarray(tokens, dtype=np.int32)
+        val = np.asarray(slots, dtype=np.int32)
+        assert key.size == val.size
+        matched, node = self.match_prefix(key)
+        k = matched.size
+        if k < key.size:
+            leaf = _Node(key[k:].copy(), val[k:].copy(), node)
+            leaf.last_access = self._tick()
+            node.children[int(leaf.key[0])] = leaf
+        return k
+
+    def path(self, tokens: Sequence[int]) -> List[_Node]:
+        """Nodes along the cached prefix of tokens (after splitting at its end)."""
+        _, node = self.match_prefix(tokens)
+        out = []
+        while node is not self.root:
+            out.append(node)
+            node = node.parent
+        return out[::-1]
+
+    # ------------------------------------------------------------------ references
+    def lock(self, node: _Node) -> None:
+        while node is not None:
+            node.lock_ref += 1
+            node = node.parent
+
+    def unlock(self, node: _Node) -> None:
+        while node is not None:
+            node.lock_ref -= 1
+            assert node.lock_ref >= 0
+            node = node.parent
+
+    # ------------------------------------------------------------------ eviction
+    def _leaves(self) -> List[_Node]:
+        out, stack = [], [self.root]
+        while stack:
+            n = stack.pop()
+            if not n.children and n is not self.root:
+                out.append(n)
+            stack.extend(n.children.values())
+        return out
+
+    def evict(self, num_tokens: int) -> int:
+        """Free at least num_tokens slots by removing unreferenced leaves, least recently used first.
+        Returns the number of slots freed (less if everything left is referenced)."""
+        heap = [(n.last_access, n.uid, n) for n in self._leaves() if n.lock_ref == 0]
+        heapq.heapify(heap)
+        freed = 0
+        while freed < num_tokens and heap:
+            _, _, leaf = heapq.heappop(heap)
+            self.pool.free(leaf.value)
+            freed += leaf.value.size
+            parent = leaf.parent
+            del parent.children[int(leaf.key[0])]
+            if parent is not self.root and not parent.children and parent.lock_ref == 0:
+                heapq.heappush(heap, (parent.last_access, parent.uid, parent))
+        return freed
+
+    # ------------------------------------------------------------------ sizes
+    def total_tokens(self) -> int:
+        total, stack = 0, [self.root]
+        while stack:
+            n = stack.pop()
+            total += n.key.size
+            stack.extend(n.children.values())
+        return total
+
+    def edges(self) -> List[Tuple[Tuple[int, ...], Tuple[int, ...]]]:
+        """(tokens of the parent path, tokens of the edge) for every node: a canonical view of the tree."""
+        out, stack = [], [(self.root, ())]
+        while stack:
+            n, prefix = stack.pop()
+            for c in n.children.values():
+                e = tuple(int(x) for x in c.key.tolist())
+                out.append((prefix, e))
+                stack.append((c, prefix + e))
+        return sorted(out)
+
+
+def cascade_groups(paths: Sequence[Sequence[int]], min_prefix: int = 1,
+                   min_members: int = 2) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """One-level cascade groups for a decode batch from its table rows.
+
+    paths[b] is request b's slot row (context order).  Requests are grouped by
+    their first slot (the subtree under the root they belong to); a group's
+    prefix is the longest run of slots all its members share, capped so that
+    every member keeps its last (new) token private.  Groups below min_members
+    or min_prefix are dropped.  Returns (group_indptr, group_reqs,
+    group_prefix_len) for ra_decode_attention.
+    """
+    by_first: Dict[int, List[int]] = {}
+    for b, row in enumerate(paths):
+        if len(row):
+            by_first.setdefault(int(row[0]), []).append(b)
+    indptr, reqs, plens = [0], [], []
+    for _, members in sorted(by_first.items()):
+        if len(members) < min_members:
+            continue
+        rows = [np.asarray(paths[b]) for b in members]
+        plen = min(r.size - 1 for r in rows)
+        lead = rows[0]
+        for r in rows[1:]:
+            plen = min(plen, _common_len(lead, r))
+        if plen < min_prefix:
+            continue
+        reqs.extend(members)
+        indptr.append(len(reqs))
+        plens.append(plen)
+    return (np.asarray(indptr, np.int32), np.asarray(reqs, np.int32), np.asarray(plens, np.int32))

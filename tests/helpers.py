@@ -107,3 +107,11 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str):
         raise AssertionError(f"{what}: {bad.sum()} of {bad.size} elements outside 1e-2 + 1e-2|ref| "
                              f"(max err {err.max():.3e}; first at {tuple(i)}: got {got[tuple(i)]}, "
                              f"ref {ref[tuple(i)]})")
+
+
+def attach_tree_groups(b: W.Batch, min_prefix: int = 256) -> W.Batch:
+    """Give a decode batch the one-level cascade groups the radix tree derives from its table rows."""
+    from prefix_shared_kv_ra_gb300.radix import cascade_groups
+    rows = [b.req_to_token[r, :L] for r, L in zip(b.dec_rpi, b.dec_seq_lens)]
+    b.casc_group_indptr, b.casc_group_reqs, b.casc_group_prefix_len = cascade_groups(rows, min_prefix=min_prefix)
+    return b

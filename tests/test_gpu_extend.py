@@ -7,7 +7,7 @@ import torch
 import oracle
 import prefix_shared_kv_ra_gb300 as ra
 import workloads as W
-from helpers import DeviceBatch, assert_close, to_f64
+from helpers import DeviceBatch, assert_close, attach_tree_groups, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -159,3 +159,14 @@ def test_cascade_member_without_private_keys():
     db = DeviceBatch(b)
     db.store()
     check_cascade(db)
+
+
+def test_cascade_multiturn_mix_tree_groups_sampled():
+    """The multi-turn mix's decode with one-level groups derived by the radix tree (prefixes up to ~14K)."""
+    b = attach_tree_groups(W.cfg5_multiturn_mix_70b())
+    assert b.has_cascade()
+    db = DeviceBatch(b)
+    db.store()
+    rng = np.random.default_rng(5)
+    sel = np.sort(rng.choice(b.n_decode * b.num_q_heads, size=384, replace=False))
+    check_cascade(db, sel=sel)
