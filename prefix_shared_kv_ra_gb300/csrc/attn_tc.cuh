@@ -96,6 +96,14 @@ constexpr int kGroups = kKeys / 4;          // 4-key gather groups per tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kFastSumLimit = 32768.0f;  // single-pass acceptance: every p of the row <= 2^15
+// Register split: the softmax warpgroups (0, 1) hold a 128-key P row and two 32-column S chunks; the
+// gather and MMA warpgroups (2, 3) need few.  setmaxnreg moves registers between them within the
+// block's launch allocation (kThreads x kLaunchRegs), which the split must add up to exactly.
+constexpr int kLaunchRegs = 65536 / kThreads;  // what __launch_bounds__(kThreads, 1) compiles to
+constexpr int kSoftmaxRegs = 184;
+constexpr int kOtherRegs = 72;
+static_assert(2 * 128 * kSoftmaxRegs + 2 * 128 * kOtherRegs == kThreads * kLaunchRegs, "register split");
 
 template <int D, int KS, int VS>
 struct Layout {
@@ -243,6 +251,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 
   if (warp >= kKWarp0 && warp < kMmaWarp) {
     // ================================================================ producers (TMA)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
     const bool is_v = warp >= kVWarp0;
     const int nw = is_v ? kVWarps : kKWarps;
     const int pw = warp - (is_v ? kVWarp0 : kKWarp0);  // 0 .. nw-1
@@ -347,6 +356,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       mbar_wait(smem_u32(&full[j % ns]), (j / ns) & 1);
   } else if (warp == kMmaWarp) {
     // ================================================================ MMA issuer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kRows, kKeys, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, D, 0, 1);
@@ -404,6 +414,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     __syncwarp();
   } else {
     // ================================================================ softmax (warps 0-7)
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     const int ti = warp >> 2;              // query tile
     const int r = threadIdx.x & 127;        // row of the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -422,81 +433,97 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       tc_fence_after();
       const int32_t key0 = kbeg + j * kKeys;
       const bool masked = key0 + kKeys > lim;
-      // pass 1: row max of the raw scores (scale > 0 commutes with max), 8 independent chains; the next
-      // 32-column TMEM load is in flight while the current chunk is reduced
-      float mx8[8];
+      // Tiles after the first are exponentiated against the current reference in a single pass.  The
+      // row sum bounds every probability of the row (p <= sum), so a sum above kFastSumLimit, or one
+      // that is not finite, marks the reference as stale: the warp then redoes the tile on the exact
+      // path -- row maximum first, lazy reference update, then the exponentials -- which the first
+      // tile always takes.  P is held in registers until the pass is accepted, since it overwrites S.
+      uint32_t pk[2][32];
+      float rowsum = 0.f, alpha = 1.f, m_ref = m_used;
+      bool resc = false;
+      bool exact = j == 0;
+#pragma unroll 1
+      for (int attempt = 0; attempt < 2; ++attempt) {
+        if (exact) {
+          // row max of the raw scores (scale > 0 commutes with max), 8 independent chains; the next
+          // 32-column TMEM load is in flight while the current chunk is reduced
+          float mx8[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-      auto max_chunk = [&](const uint32_t (&sr)[32], int c) {
+          for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+          auto max_chunk = [&](const uint32_t (&sr)[32], int c) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float x = (masked && key0 + c * 32 + e >= lim) ? -INFINITY : __uint_as_float(sr[e]);
-          mx8[e & 7] = fmaxf(mx8[e & 7], x);
+            for (int e = 0; e < 32; ++e) {
+              const float x = (masked && key0 + c * 32 + e >= lim) ? -INFINITY : __uint_as_float(sr[e]);
+              mx8[e & 7] = fmaxf(mx8[e & 7], x);
+            }
+          };
+          uint32_t ba[32], bb[32];
+          tmem_ld32(tmem + lane_addr + col_s, ba);
+          tc_wait_ld_regs(ba);
+          tmem_ld32(tmem + lane_addr + col_s + 32, bb);
+          max_chunk(ba, 0);
+          tc_wait_ld_regs(bb);
+          tmem_ld32(tmem + lane_addr + col_s + 64, ba);
+          max_chunk(bb, 1);
+          tc_wait_ld_regs(ba);
+          tmem_ld32(tmem + lane_addr + col_s + 96, bb);
+          max_chunk(ba, 2);
+          tc_wait_ld_regs(bb);
+          max_chunk(bb, 3);
+          const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.scale_log2;
+          const float m_new = fmaxf(m_used, mx);
+          resc = m_new > m_used + kRescaleThreshold;
+          m_ref = resc ? m_new : m_used;
         }
-      };
-      {
-        uint32_t ba[32], bb[32];
-        tmem_ld32(tmem + lane_addr + col_s, ba);
-        tc_wait_ld_regs(ba);
-        tmem_ld32(tmem + lane_addr + col_s + 32, bb);
-        max_chunk(ba, 0);
-        tc_wait_ld_regs(bb);
-        tmem_ld32(tmem + lane_addr + col_s + 64, ba);
-        max_chunk(bb, 1);
-        tc_wait_ld_regs(ba);
-        tmem_ld32(tmem + lane_addr + col_s + 96, bb);
-        max_chunk(ba, 2);
-        tc_wait_ld_regs(bb);
-        max_chunk(bb, 3);
-      }
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.scale_log2;
-      const float m_new = fmaxf(m_used, mx);
-      const bool resc = m_new > m_used + kRescaleThreshold;
-      const float m_ref = resc ? m_new : m_used;
-      const float m_sub = (m_ref == -INFINITY) ? 0.f : m_ref;
-      const float alpha = resc ? ex2(m_used - m_sub) : 1.f;
-      // pass 2: p = 2^(s * scale_log2 - m_ref): packed FMA pairs + one MUFU per score, packed to bf16 over S
-      const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
-      const uint64_t neg_m2 = f2_pack(-m_sub, -m_sub);
-      uint64_t sum2[4] = {0, 0, 0, 0};  // 4 independent chains of (even, odd) partial sums
-      auto exp_chunk = [&](const uint32_t (&sr)[32], int c) {
-        uint32_t pk[16];
+        const float m_sub = (m_ref == -INFINITY) ? 0.f : m_ref;
+        alpha = resc ? ex2(m_used - m_sub) : 1.f;
+        // p = 2^(s * scale_log2 - m_ref): packed FMA pairs + one MUFU per score, packed to bf16 pairs
+        const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
+        const uint64_t neg_m2 = f2_pack(-m_sub, -m_sub);
+        uint64_t sum2[4] = {0, 0, 0, 0};  // 4 independent chains of (even, odd) partial sums
+        auto exp_chunk = [&](const uint32_t (&sr)[32], int c) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float s0 = __uint_as_float(sr[2 * e]), s1 = __uint_as_float(sr[2 * e + 1]);
-          if (masked) {
-            if (key0 + c * 32 + 2 * e >= lim) s0 = -INFINITY;
-            if (key0 + c * 32 + 2 * e + 1 >= lim) s1 = -INFINITY;
+          for (int e = 0; e < 16; ++e) {
+            float s0 = __uint_as_float(sr[2 * e]), s1 = __uint_as_float(sr[2 * e + 1]);
+            if (masked) {
+              if (key0 + c * 32 + 2 * e >= lim) s0 = -INFINITY;
+              if (key0 + c * 32 + 2 * e + 1 >= lim) s1 = -INFINITY;
+            }
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(s0, s1), scale2, neg_m2), t0, t1);
+            const float p0 = ex2(t0), p1 = ex2(t1);
+            sum2[e & 3] = f2_add(sum2[e & 3], f2_pack(p0, p1));
+            pk[c >> 1][(c & 1) * 16 + e] = pack_bf16x2(p0, p1);
           }
-          float t0, t1;
-          f2_unpack(f2_fma(f2_pack(s0, s1), scale2, neg_m2), t0, t1);
-          const float p0 = ex2(t0), p1 = ex2(t1);
-          sum2[e & 3] = f2_add(sum2[e & 3], f2_pack(p0, p1));
-          pk[e] = pack_bf16x2(p0, p1);
+        };
+        {
+          uint32_t ba[32], bb[32];
+          tmem_ld32(tmem + lane_addr + col_s, ba);
+          tc_wait_ld_regs(ba);
+          tmem_ld32(tmem + lane_addr + col_s + 32, bb);
+          exp_chunk(ba, 0);
+          tc_wait_ld_regs(bb);
+          tmem_ld32(tmem + lane_addr + col_s + 64, ba);
+          exp_chunk(bb, 1);
+          tc_wait_ld_regs(ba);
+          tmem_ld32(tmem + lane_addr + col_s + 96, bb);
+          exp_chunk(ba, 2);
+          tc_wait_ld_regs(bb);
+          exp_chunk(bb, 3);
         }
-        // P columns 16c .. 16c+15 overwrite S columns already read
-        tmem_st16(tmem + lane_addr + col_s + c * 16, pk);
-      };
-      {
-        uint32_t ba[32], bb[32];
-        tmem_ld32(tmem + lane_addr + col_s, ba);
-        tc_wait_ld_regs(ba);
-        tmem_ld32(tmem + lane_addr + col_s + 32, bb);
-        exp_chunk(ba, 0);  // writes P columns 0..15: S chunk 0, already in registers
-        tc_wait_ld_regs(bb);
-        tmem_ld32(tmem + lane_addr + col_s + 64, ba);
-        exp_chunk(bb, 1);  // P columns 16..31
-        tc_wait_ld_regs(ba);
-        tmem_ld32(tmem + lane_addr + col_s + 96, bb);
-        exp_chunk(ba, 2);  // P columns 32..47: S chunk 1, already read
-        tc_wait_ld_regs(bb);
-        exp_chunk(bb, 3);  // P columns 48..63
-      }
-      float sum8[8];
+        float sum8[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) f2_unpack(sum2[e], sum8[2 * e], sum8[2 * e + 1]);
-      const float rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        for (int e = 0; e < 4; ++e) f2_unpack(sum2[e], sum8[2 * e], sum8[2 * e + 1]);
+        rowsum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        if (exact) break;
+        const bool stale = !(rowsum <= kFastSumLimit);
+        if (!__any_sync(0xffffffffu, stale)) break;
+        exact = true;
+      }
+      // P (bf16 pairs) over the first 64 columns of S, read by the PV MMA
+      tmem_st32(tmem + lane_addr + col_s, pk[0]);
+      tmem_st32(tmem + lane_addr + col_s + 32, pk[1]);
       l = l * alpha + rowsum;
       if (j > 0) {
         // Observe PV_{j-1} before releasing P_j: bar_o then never runs two phases ahead of

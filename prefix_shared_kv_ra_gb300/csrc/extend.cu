@@ -59,10 +59,19 @@ ra_status row_gather_map(CUtensorMap* map, const void* base, int64_t rows, int32
   return RA_OK;
 }
 
+// Opt the kernel into its dynamic shared memory and check that it was compiled to the per-thread
+// register count its setmaxnreg split is balanced against (a split above the block's launch
+// allocation would leave the softmax warps waiting for registers that never come).
 template <typename Kern>
 ra_status set_smem(Kern kern, int bytes, bool* configured, int device) {
   if (configured[device]) return RA_OK;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaFuncGetAttributes(attn_tc): %s", cudaGetErrorString(e));
+  if (fa.numRegs != tc::kLaunchRegs)
+    return fail(RA_ERR_UNSUPPORTED, "attn_tc kernel compiled to %d registers per thread, its register split needs %d",
+                fa.numRegs, tc::kLaunchRegs);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaFuncSetAttribute(attn_tc): %s", cudaGetErrorString(e));
   configured[device] = true;
   return RA_OK;

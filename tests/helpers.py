@@ -115,3 +115,24 @@ def attach_tree_groups(b: W.Batch, min_prefix: int = 256) -> W.Batch:
     rows = [b.req_to_token[r, :L] for r, L in zip(b.dec_rpi, b.dec_seq_lens)]
     b.casc_group_indptr, b.casc_group_reqs, b.casc_group_prefix_len = cascade_groups(rows, min_prefix=min_prefix)
     return b
+
+
+def grow_key_scale(b: W.Batch, per_tile: float = 6.0, tile: int = 128) -> W.Batch:
+    """Scale every key by 1 + per_tile * (its context position // tile), in place: scores then grow from
+    one 128-key tile to the next by far more than any lazy softmax reference allows, so kernels that
+    exponentiate against a running reference must move it (and rescale O) on every tile."""
+    pos = {}
+    rows = [(r, int(n)) for r, n in zip(b.ext_rpi, b.ext_prefix_lens + b.ext_extend_lens)] + \
+           [(r, int(n)) for r, n in zip(b.dec_rpi, b.dec_seq_lens)]
+    for r, n in rows:
+        for p, s in enumerate(b.req_to_token[r, :n].tolist()):
+            pos[s] = p
+
+    def scaled(bits: np.ndarray, slots: np.ndarray) -> np.ndarray:
+        f = np.array([1.0 + per_tile * (pos.get(int(s), 0) // tile) for s in slots], dtype=np.float32)
+        x = W.bf16_bits_to_f32(bits) * f[:, None, None]
+        return W.f32_to_bf16_bits(x)
+
+    b.pool_k = scaled(b.pool_k, b.pool_slots)
+    b.k_new = scaled(b.k_new, b.out_cache_loc)
+    return b

@@ -7,7 +7,7 @@ import torch
 import oracle
 import prefix_shared_kv_ra_gb300 as ra
 import workloads as W
-from helpers import DeviceBatch, assert_close, attach_tree_groups, to_f64
+from helpers import DeviceBatch, assert_close, attach_tree_groups, grow_key_scale, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -46,6 +46,17 @@ def test_extend_prefix_zero_and_single_token_suffix():
     b = W.random_mixed(11, n_extend=5, n_decode=0, num_q_heads=32, num_kv_heads=8, head_dim=128, max_len=300,
                        share_prob=0.0, ext_lens=[1, 300, 1, 129, 128])
     assert (b.ext_prefix_lens == 0).any() and (b.ext_extend_lens == 1).any()
+    db = DeviceBatch(b)
+    db.store()
+    check_extend(db)
+
+
+@pytest.mark.parametrize("seed,hq,hkv,d", [(21, 32, 8, 128), (22, 16, 2, 64)])
+def test_extend_growing_scores(seed, hq, hkv, d):
+    """Scores that grow by orders of magnitude from tile to tile: every tile after the first fails the
+    single-pass acceptance bound and is redone with the exact maximum and an O rescale."""
+    b = grow_key_scale(W.random_mixed(seed, n_extend=5, n_decode=0, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                                      max_len=700, min_len=300))
     db = DeviceBatch(b)
     db.store()
     check_extend(db)
@@ -170,3 +181,12 @@ def test_cascade_multiturn_mix_tree_groups_sampled():
     rng = np.random.default_rng(5)
     sel = np.sort(rng.choice(b.n_decode * b.num_q_heads, size=384, replace=False))
     check_cascade(db, sel=sel)
+
+
+def test_cascade_growing_scores():
+    """The prefix pass's tiles (several per split) under scores that grow tile by tile."""
+    b = grow_key_scale(W.cfg2_decode_8b())  # 8 groups sharing 1024 prompt tokens: 512-key splits of 4 tiles
+    assert b.has_cascade()
+    db = DeviceBatch(b)
+    db.store()
+    check_cascade(db)
