@@ -134,8 +134,12 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   using L = Layout<D, KS, VS>;
   constexpr int HALVES = D / 64;  // 128-byte (64-element) column blocks of a row
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_q, bar_kf[KS], bar_ke[KS], bar_vf[VS], bar_ve[VS], bar_s[kTiles],
-      bar_p[kTiles], bar_o[kTiles], bar_done;
+  // K/V stage release: one barrier per key tile t (ring of KVF), committed after the last MMA reading
+  // K_t and V_t (PV of query tile 1).  KVF > max(KS, VS): a producer waiting for tile t's release
+  // cannot see the ring slot complete tile t + KVF first (that tile needs its own next copy).
+  constexpr int KVF = (KS > VS ? KS : VS) + 1;
+  __shared__ __align__(8) uint64_t bar_q, bar_kf[KS], bar_vf[VS], bar_kvfree[KVF], bar_s[kTiles], bar_p[kTiles],
+      bar_o[kTiles], bar_done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -219,14 +223,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   if (threadIdx.x == 0) {
     s_abort = 0;
     mbar_init(smem_u32(&bar_q), EXTEND ? 1 : kKWarps);
-    for (int s = 0; s < KS; ++s) {
-      mbar_init(smem_u32(&bar_kf[s]), kKWarps);
-      mbar_init(smem_u32(&bar_ke[s]), 1);
-    }
-    for (int s = 0; s < VS; ++s) {
-      mbar_init(smem_u32(&bar_vf[s]), kVWarps);
-      mbar_init(smem_u32(&bar_ve[s]), 1);
-    }
+    for (int s = 0; s < KS; ++s) mbar_init(smem_u32(&bar_kf[s]), kKWarps);
+    for (int s = 0; s < VS; ++s) mbar_init(smem_u32(&bar_vf[s]), kVWarps);
+    for (int s = 0; s < KVF; ++s) mbar_init(smem_u32(&bar_kvfree[s]), 1);
     for (int i = 0; i < kTiles; ++i) {
       mbar_init(smem_u32(&bar_s[i]), 1);
       mbar_init(smem_u32(&bar_p[i]), 128);
@@ -307,7 +306,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     const int g0 = pw * kGroups / nw, g1 = (pw + 1) * kGroups / nw;
     const int nkeys = 4 * (g1 - g0);  // <= 44
     uint64_t* full = is_v ? bar_vf : bar_kf;
-    uint64_t* empty = is_v ? bar_ve : bar_ke;
+
     const int ns = is_v ? VS : KS;
     auto load_row = [&](int j, int k) -> int32_t {  // tensor-map row (slot * Hkv + kh) of key 4*g0 + k
       if (k >= nkeys) return 0;
@@ -326,7 +325,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       const int st = j % ns;
       const int32_t na = j + 1 < nt ? load_row(j + 1, lane) : 0;
       const int32_t nb = j + 1 < nt ? load_row(j + 1, lane + 32) : 0;
-      if (j >= ns && !mbar_wait(smem_u32(&empty[st]), ((j / ns) + 1) & 1)) {
+      // stage st held tile j - ns: wait for that tile's release
+      if (j >= ns && !mbar_wait(smem_u32(&bar_kvfree[(j - ns) % KVF]), ((j - ns) / KVF) & 1)) {
         give_up();
         break;
       }
@@ -378,7 +378,6 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
                     idesc_qk, kk > 0);
         }
         tc_commit(smem_u32(&bar_s[i]));
-        if (i == kTiles - 1) tc_commit(smem_u32(&bar_ke[st]));
         issued = true;
         return true;
       };
@@ -396,8 +395,10 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
           tc_mma_ts(tmem + kColO + i * 128, tmem + i * kKeys + kk * 8,
                     sdesc_sw128(sV(st) + kk * 2048, kRows * 128, 1024), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(smem_u32(&bar_o[i]));
-        if (i == kTiles - 1) tc_commit(smem_u32(&bar_ve[st]));
+        // Each commit stalls the tensor pipe briefly, so there are three per key tile: S_0, S_1 and the
+        // K/V release here.  O_i needs none until the last tile: S_i(j+1)'s commit also covers PV_i(j).
+        if (i == kTiles - 1) tc_commit(smem_u32(&bar_kvfree[j % KVF]));
+        if (j == nt - 1) tc_commit(smem_u32(&bar_o[i]));
         return true;
       };
       ok = ok && qk(0, 0) && qk(1, 0);
@@ -526,10 +527,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       tmem_st32(tmem + lane_addr + col_s + 32, pk[1]);
       l = l * alpha + rowsum;
       if (j > 0) {
-        // Observe PV_{j-1} before releasing P_j: bar_o then never runs two phases ahead of
-        // this warp's parity waits, and O is complete for tile j-1 if it must be rescaled.
-        const bool late = !mbar_wait(smem_u32(&bar_o[ti]), (j - 1) & 1);
-        if (__any_sync(0xffffffffu, late)) { ok = false; break; }
+        // O_i holds PV_i(j-1): the commit that signalled S_i(j) covers every earlier MMA
         if (__any_sync(0xffffffffu, resc)) {
           tc_fence_after();
 #pragma unroll 1
@@ -550,7 +548,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     }
     if (!ok) give_up();
     // ---- epilogue: O / l
-    ok = ok && mbar_wait(smem_u32(&bar_o[ti]), (nt - 1) & 1);
+    ok = ok && mbar_wait(smem_u32(&bar_o[ti]), 0);  // committed once, after the last PV
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
       const float inv_l = 1.f / l;
