@@ -215,6 +215,8 @@ class Step:
                                            self.casc.get("max_group_prefix_len", 0),
                                            self.casc.get("max_group_size", 0))
         self.ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
+        self.ext_ws = torch.empty(max(ra.ra_extend_workspace_bytes(b.n_extend, b.total_q_extend, b.num_q_heads, hkv),
+                                      256), dtype=torch.uint8, device=dev)
         # kernel launches per step (the library's launch structure)
         # kernel launches per step: store, extend, [key_start scatter, prefix pass,] decode, combine
         self.launches = 1 + (1 if b.n_extend else 0) + ((2 + (2 if self.cascade else 0)) if b.n_decode else 0)
@@ -231,7 +233,8 @@ class Step:
         if b.n_extend:
             ra.ra_extend_attention(self.k_pool, self.v_pool, d["ext_q"], self.ext_o, self.table, d["ext_rpi"],
                                    d["ext_prefix"], d["ext_len"], d["ext_qo"], max_extend_len=b.max_extend_len,
-                                   max_prefix_len=b.max_prefix_len, sm_scale=b.sm_scale, device_error=self.err)
+                                   max_prefix_len=b.max_prefix_len, sm_scale=b.sm_scale, workspace=self.ext_ws,
+                                   device_error=self.err)
         if ev[2] is not None:
             ev[2].record()
         if b.n_decode:

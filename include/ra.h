@@ -103,6 +103,20 @@ ra_status ra_kv_store(void* k_pool, void* v_pool, int64_t num_slots, int32_t num
  * The suffix keys must already be stored (ra_kv_store) and listed in the table.
  * Rows with extend_lens[b] == 0 write nothing; prefix_lens[b] == 0 is plain
  * causal attention.  batch == 0 or total_q == 0 is a no-op.
+ *   workspace:       device scratch of at least ra_extend_workspace_bytes(batch,
+ *                    total_q, num_q_heads, num_kv_heads) bytes, 16-byte aligned
+ *                    (may be NULL when batch or total_q is 0); it holds the
+ *                    work list of (request, query tile) pairs, ordered longest
+ *                    key range first, that a one-CTA pass builds on the stream
+ *                    before the attention kernel runs.  Smaller: RA_ERR_WORKSPACE.
+ *                    The contents are scratch; calls that overlap on the GPU
+ *                    need separate workspaces.
+ * The suffix keys must already be stored (ra_kv_store) and listed in the table.
+ * Rows with extend_lens[b] == 0 write nothing; prefix_lens[b] == 0 is plain
+ * causal attention.  batch == 0 or total_q == 0 is a no-op.  A request with
+ * prefix_lens[b] + extend_lens[b] > table_stride is flagged RA_DEVERR_LENGTH and
+ * skipped; the sum of extend_lens must not exceed total_q (excess tiles are
+ * flagged RA_DEVERR_LENGTH and skipped).
  * Runs on tcgen05 tensor cores with TMEM accumulators; K/V rows are gathered
  * from the pool into 128B-swizzled shared-memory tiles, the query tile comes
  * in by one TMA tile load.
@@ -112,8 +126,11 @@ ra_status ra_extend_attention(const void* k_pool, const void* v_pool, int64_t nu
                               const int32_t* req_to_token, int64_t table_stride, int64_t table_rows,
                               const int32_t* req_pool_indices, const int32_t* prefix_lens,
                               const int32_t* extend_lens, const int32_t* qo_indptr, int32_t batch, int64_t total_q,
-                              int32_t max_extend_len, int32_t max_prefix_len, uint32_t* device_error,
-                              ra_stream_t stream);
+                              int32_t max_extend_len, int32_t max_prefix_len, void* workspace,
+                              size_t workspace_bytes, uint32_t* device_error, ra_stream_t stream);
+
+/* Workspace bytes ra_extend_attention needs (0 for invalid head counts). */
+size_t ra_extend_workspace_bytes(int32_t batch, int64_t total_q, int32_t num_q_heads, int32_t num_kv_heads);
 
 /*
  * ra_decode_attention -- one new query token per request over its context.
@@ -194,7 +211,7 @@ const char* ra_last_error_message(void);
 /* ABI revision of this header (bumped on any signature change). */
 int32_t ra_abi_version(void);
 
-#define RA_ABI_VERSION 1
+#define RA_ABI_VERSION 2
 
 #ifdef __cplusplus
 }

@@ -22,7 +22,8 @@ import torch
 
 from . import _build
 
-__all__ = ["RAError", "ra_kv_store", "ra_extend_attention", "ra_decode_attention", "ra_decode_workspace_bytes",
+__all__ = ["RAError", "ra_kv_store", "ra_extend_attention", "ra_extend_workspace_bytes", "ra_decode_attention",
+           "ra_decode_workspace_bytes",
            "ra_decode_attention_static", "RA_DECODE_STATIC_SCRATCH_BYTES",
            "ra_abi_version", "library_path", "load", "DEVERR_SLOT", "DEVERR_TABLE", "DEVERR_LENGTH",
            "DEVERR_TIMEOUT"]
@@ -56,7 +57,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     lib.ra_kv_store.argtypes = [P, P, i64, i32, i32, P, P, P, i64, P, P]
     lib.ra_extend_attention.argtypes = [P, P, i64, i32, i32, P, P, i32, f32, P, i64, i64, P, P, P, P, i32, i64,
-                                        i32, i32, P, P]
+                                        i32, i32, P, sz, P, P]
+    lib.ra_extend_workspace_bytes.argtypes = [i32, i64, i32, i32]
+    lib.ra_extend_workspace_bytes.restype = sz
     lib.ra_decode_attention.argtypes = [P, P, i64, i32, i32, P, P, i32, f32, P, i64, i64, P, P, i32, i32, i32,
                                         P, P, P, i32, i32, P, sz, P, P]
     lib.ra_decode_attention_static.argtypes = [P, P, i64, i32, i32, P, P, i32, f32, P, i64, i64, P, P, i32, i32,
@@ -120,9 +123,10 @@ def ra_kv_store(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch.Tensor,
 def ra_extend_attention(k_pool: torch.Tensor, v_pool: torch.Tensor, q: torch.Tensor, o: torch.Tensor,
                         req_to_token: torch.Tensor, req_pool_indices: torch.Tensor, prefix_lens: torch.Tensor,
                         extend_lens: torch.Tensor, qo_indptr: torch.Tensor, *, max_extend_len: int,
-                        max_prefix_len: int, sm_scale: float, device_error: Optional[torch.Tensor] = None,
-                        stream=None) -> None:
-    """Suffix queries over cached prefix + causal suffix; q, o [total_q, Hq, D] bf16."""
+                        max_prefix_len: int, sm_scale: float, workspace: torch.Tensor,
+                        device_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Suffix queries over cached prefix + causal suffix; q, o [total_q, Hq, D] bf16; workspace: uint8,
+    at least ra_extend_workspace_bytes(batch, total_q, Hq, Hkv) bytes."""
     dev = k_pool.device
     S, hkv, d = k_pool.shape
     total_q, hq, dq = q.shape
@@ -130,13 +134,20 @@ def ra_extend_attention(k_pool: torch.Tensor, v_pool: torch.Tensor, q: torch.Ten
         raise ValueError("q/o shape mismatch")
     batch = req_pool_indices.shape[0]
     bf, i32 = torch.bfloat16, torch.int32
+    if workspace.dtype != torch.uint8 or not workspace.is_contiguous() or workspace.device != dev:
+        raise ValueError("workspace must be a contiguous uint8 tensor on the pool's device")
     _check(load().ra_extend_attention(
         _ptr(k_pool, bf, "k_pool", dev), _ptr(v_pool, bf, "v_pool", dev), S, hkv, d, _ptr(q, bf, "q", dev),
         _ptr(o, bf, "o", dev), hq, float(sm_scale), _ptr(req_to_token, i32, "req_to_token", dev),
         req_to_token.shape[1], req_to_token.shape[0], _ptr(req_pool_indices, i32, "req_pool_indices", dev),
         _ptr(prefix_lens, i32, "prefix_lens", dev), _ptr(extend_lens, i32, "extend_lens", dev),
         _ptr(qo_indptr, i32, "qo_indptr", dev), batch, total_q, int(max_extend_len), int(max_prefix_len),
-        _ptr(device_error, i32, "device_error", dev), _stream(dev, stream)))
+        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _ptr(device_error, i32, "device_error", dev),
+        _stream(dev, stream)))
+
+
+def ra_extend_workspace_bytes(batch: int, total_q: int, num_q_heads: int, num_kv_heads: int) -> int:
+    return int(load().ra_extend_workspace_bytes(batch, total_q, num_q_heads, num_kv_heads))
 
 
 def ra_decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, max_seq_len: int,

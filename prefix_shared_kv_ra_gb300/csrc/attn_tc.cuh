@@ -69,6 +69,8 @@ struct TcParams {
   int32_t max_extend_len;
   int32_t max_prefix_len;
   __nv_bfloat16* o;
+  const int32_t* work_count;  // number of (request, query tile) entries in work_items
+  const int32_t* work_items;  // [2 * entries]: request, query tile; longest key range first
   // cascade prefix pass
   const int32_t* group_indptr;
   const int32_t* group_reqs;
@@ -149,7 +151,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int G = p.group;
   const int T = kRows / G;  // tokens (or members) per query tile
-  const int kh = blockIdx.y;
+  const int kh = EXTEND ? static_cast<int>(blockIdx.x % p.hkv) : static_cast<int>(blockIdx.y);
 
   // ------------------------------------------------------------------ job (CTA-uniform)
   int32_t kbeg = 0, kend = 0, table_row = 0;
@@ -159,17 +161,16 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   int32_t mem0 = 0;      // cascade: first member index into group_reqs
   int32_t csplit = 0;
   if constexpr (EXTEND) {
-    const int b = blockIdx.z;
-    const int tile = blockIdx.x;
-    int32_t E = __ldg(p.extend_lens + b);
+    // entry blockIdx.x / Hkv of the work list (the kv heads of an entry are adjacent CTAs: they read
+    // the same slots' rows at the same time); the list holds only valid, non-empty query tiles
+    // (lengths were checked and flagged when it was built)
+    const int32_t entry = static_cast<int32_t>(blockIdx.x / p.hkv);
+    if (entry >= __ldg(p.work_count)) return;
+    const int b = __ldg(p.work_items + 2 * entry);
+    const int tile = __ldg(p.work_items + 2 * entry + 1);
+    const int32_t E = min(max(__ldg(p.extend_lens + b), 0), p.max_extend_len);
     const int32_t P = __ldg(p.prefix_lens + b);
     table_row = __ldg(p.rpi + b);
-    if (E > p.max_extend_len || P > p.max_prefix_len || E < 0 || P < 0) {
-      if (tile == 0 && kh == 0 && threadIdx.x == 0) flag_error(p.err, RA_DEVERR_LENGTH);
-      E = min(max(E, 0), p.max_extend_len);
-      if (P < 0 || P > p.max_prefix_len) return;
-    }
-    if (tile * kTiles * T >= E) return;
     if (table_row < 0 || table_row >= p.table_rows) {
       if (tile == 0 && kh == 0 && threadIdx.x == 0) flag_error(p.err, RA_DEVERR_TABLE);
       return;
@@ -178,10 +179,6 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     causal0 = P + tile * kTiles * T;
     kbeg = 0;
     kend = causal0 + n_valid;
-    if (kend > p.table_stride) {
-      if (tile == 0 && kh == 0 && threadIdx.x == 0) flag_error(p.err, RA_DEVERR_LENGTH);
-      return;
-    }
     q_tok0 = static_cast<int64_t>(__ldg(p.qo_indptr + b)) + tile * kTiles * T;
   } else {
     const int g = blockIdx.z;

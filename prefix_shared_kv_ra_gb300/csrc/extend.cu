@@ -22,6 +22,122 @@ namespace ra {
 
 namespace {
 
+// ------------------------------------------------------------------ work list
+// The extend CTAs of a batch differ in length by two orders of magnitude (a query tile of a request
+// with a 32K-token prefix sweeps 256 key tiles, one of a fresh request a single tile).  Launched in
+// (tile, head, request) order, the longest can start last and leave most SMs idle at the end.  A
+// one-CTA pass lists the (request, query tile) pairs by key-tile count, longest first (a counting
+// sort); extend CTA x then takes entry x / Hkv, so the block scheduler hands out work longest first
+// (greedy LPT list scheduling) and the Hkv CTAs of an entry, which gather rows of the same slots,
+// run side by side.
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanBins = 4096;  // key-tile counts above kPlanBins - 1 share the first bin
+
+struct ExtendWorkspace {
+  int32_t* count;  // entries listed
+  int32_t* items;  // [2 * cap]
+  int64_t cap;
+  size_t total;
+};
+
+// Entries are at most sum_b ceil(E_b / tokens_per_cta) <= total_q / tokens_per_cta + batch.
+ExtendWorkspace layout_extend_workspace(int32_t batch, int64_t total_q, int32_t tokens_per_cta, void* base) {
+  ExtendWorkspace w{};
+  w.cap = (total_q + tokens_per_cta - 1) / tokens_per_cta + batch;
+  w.total = 16 + static_cast<size_t>(w.cap) * 8;
+  uint8_t* b = static_cast<uint8_t*>(base);
+  w.count = reinterpret_cast<int32_t*>(b);
+  w.items = reinterpret_cast<int32_t*>(b ? b + 16 : nullptr);
+  return w;
+}
+
+__device__ __forceinline__ int32_t plan_bin(int32_t P, int32_t E, int32_t t, int32_t tokens_per_cta) {
+  const int32_t kend = P + min(E, (t + 1) * tokens_per_cta);
+  const int32_t cost = (kend + tc::kKeys - 1) / tc::kKeys;
+  return kPlanBins - 1 - min(cost, kPlanBins - 1);  // bin 0 = longest
+}
+
+__global__ void __launch_bounds__(kPlanThreads) extend_plan_kernel(const int32_t* extend_lens,
+                                                                  const int32_t* prefix_lens, int32_t batch,
+                                                                  int32_t max_extend_len, int32_t max_prefix_len,
+                                                                  int64_t table_stride, int32_t tokens_per_cta,
+                                                                  int32_t* count, int32_t* items, int64_t cap,
+                                                                  uint32_t* err) {
+  __shared__ int32_t s_bin[kPlanBins];
+  __shared__ int32_t s_warp[kPlanThreads / 32];
+  griddep_launch();  // the extend kernel may start its launch; it waits for this grid before reading the list
+  for (int i = threadIdx.x; i < kPlanBins; i += kPlanThreads) s_bin[i] = 0;
+  __syncthreads();
+  // a request's tiles, or 0 if its lengths are invalid (flagged here, once)
+  auto tiles_of = [&](int b, int32_t& P, int32_t& E, bool report) -> int32_t {
+    E = __ldg(extend_lens + b);
+    P = __ldg(prefix_lens + b);
+    if (E < 0 || E > max_extend_len || P < 0 || P > max_prefix_len) {
+      if (report) flag_error(err, RA_DEVERR_LENGTH);
+      E = min(max(E, 0), max_extend_len);  // the rows within the bound are still computed
+      if (P < 0 || P > max_prefix_len) return 0;
+    }
+    if (static_cast<int64_t>(P) + E > table_stride) {
+      if (report) flag_error(err, RA_DEVERR_LENGTH);
+      return 0;
+    }
+    return (E + tokens_per_cta - 1) / tokens_per_cta;
+  };
+  for (int b = threadIdx.x; b < batch; b += kPlanThreads) {
+    int32_t P, E;
+    const int32_t n = tiles_of(b, P, E, true);
+    for (int32_t t = 0; t < n; ++t) atomicAdd(&s_bin[plan_bin(P, E, t, tokens_per_cta)], 1);
+  }
+  __syncthreads();
+  // exclusive scan of the bins: thread i owns bins [4i, 4i + 4)
+  constexpr int kPer = kPlanBins / kPlanThreads;
+  int32_t v[kPer], run = 0;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    v[e] = run;
+    run += s_bin[threadIdx.x * kPer + e];
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int32_t incl = run;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t w = s_warp[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    s_warp[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int32_t base = (warp > 0 ? s_warp[warp - 1] : 0) + incl - run;
+  const int32_t total = s_warp[kPlanThreads / 32 - 1];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) s_bin[threadIdx.x * kPer + e] = base + v[e];
+  __syncthreads();
+  for (int b = threadIdx.x; b < batch; b += kPlanThreads) {
+    int32_t P, E;
+    const int32_t n = tiles_of(b, P, E, false);
+    for (int32_t t = 0; t < n; ++t) {
+      const int32_t pos = atomicAdd(&s_bin[plan_bin(P, E, t, tokens_per_cta)], 1);
+      if (pos < cap) {
+        items[2 * pos] = b;
+        items[2 * pos + 1] = t;
+      } else {
+        flag_error(err, RA_DEVERR_LENGTH);  // extend_lens sum above total_q
+      }
+    }
+  }
+  if (threadIdx.x == 0) *count = static_cast<int32_t>(static_cast<int64_t>(total) < cap ? total : cap);
+  griddep_wait();  // complete only after the previous grid (the KV store): the extend kernel waits on this one
+}
+
 // K ring / V ring depths: the tensor core waits on K first, so K gets the deeper ring.
 template <int D>
 constexpr int k_stages() { return D == 128 ? 3 : 4; }
@@ -78,7 +194,7 @@ ra_status set_smem(Kern kern, int bytes, bool* configured, int device) {
 }
 
 template <int D>
-ra_status launch_extend(const TcParams& p, const CUtensorMap& qmap, int max_tiles, int batch, cudaStream_t s) {
+ra_status launch_extend(const TcParams& p, const CUtensorMap& qmap, int64_t entries, cudaStream_t s) {
   CUtensorMap kmap, vmap;
   if (ra_status st = row_gather_map(&kmap, p.k_pool, p.num_slots * p.hkv, D)) return st;
   if (ra_status st = row_gather_map(&vmap, p.v_pool, p.num_slots * p.hkv, D)) return st;
@@ -90,7 +206,7 @@ ra_status launch_extend(const TcParams& p, const CUtensorMap& qmap, int max_tile
   if (L::kDynSmem > dev.max_smem_optin)
     return fail(RA_ERR_UNSUPPORTED, "extend kernel needs %d bytes of shared memory", L::kDynSmem);
   if (ra_status st = set_smem(kern, L::kDynSmem, configured, dev.device)) return st;
-  dim3 grid(max_tiles, p.hkv, batch);
+  dim3 grid(static_cast<unsigned>(entries * p.hkv));
   return launch_pdl("attn_tc_kernel<extend>", kern, grid, dim3(tc::kThreads), L::kDynSmem, s, p, qmap, kmap, vmap);
 }
 
@@ -157,8 +273,8 @@ extern "C" ra_status ra_extend_attention(const void* k_pool, const void* v_pool,
                                          int64_t table_stride, int64_t table_rows, const int32_t* req_pool_indices,
                                          const int32_t* prefix_lens, const int32_t* extend_lens,
                                          const int32_t* qo_indptr, int32_t batch, int64_t total_q,
-                                         int32_t max_extend_len, int32_t max_prefix_len, uint32_t* device_error,
-                                         ra_stream_t stream) {
+                                         int32_t max_extend_len, int32_t max_prefix_len, void* workspace,
+                                         size_t workspace_bytes, uint32_t* device_error, ra_stream_t stream) {
   using namespace ra;
   clear_error();
   RA_REQUIRE(batch >= 0 && batch <= 65535, "batch must be in [0, 65535] (got %d)", batch);
@@ -185,6 +301,12 @@ extern "C" ra_status ra_extend_attention(const void* k_pool, const void* v_pool,
   RA_REQUIRE(aligned4(req_to_token) && aligned4(req_pool_indices) && aligned4(prefix_lens) &&
                  aligned4(extend_lens) && aligned4(qo_indptr),
              "index arrays must be 4-byte aligned");
+  const int tokens_per_cta = tc::kTiles * (128 / group);
+  const ExtendWorkspace ws = layout_extend_workspace(batch, total_q, tokens_per_cta, workspace);
+  if (!workspace || workspace_bytes < ws.total)
+    return fail(RA_ERR_WORKSPACE, "workspace of %zu bytes, need %zu", workspace ? workspace_bytes : 0, ws.total);
+  RA_REQUIRE(aligned16(workspace), "workspace must be 16-byte aligned");
+  RA_REQUIRE(ws.cap * num_kv_heads < (int64_t(1) << 31), "too many extend tiles for one grid");
 
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -222,9 +344,23 @@ extern "C" ra_status ra_extend_attention(const void* k_pool, const void* v_pool,
   p.max_extend_len = max_extend_len;
   p.max_prefix_len = max_prefix_len;
   p.o = static_cast<__nv_bfloat16*>(o);
-  const int tokens_per_cta = tc::kTiles * rows_per_tile;
-  const int max_tiles = (max_extend_len + tokens_per_cta - 1) / tokens_per_cta;
+  p.work_count = ws.count;
+  p.work_items = ws.items;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return head_dim == 128 ? launch_extend<128>(p, qmap, max_tiles, batch, s)
-                         : launch_extend<64>(p, qmap, max_tiles, batch, s);
+  if (ra_status st = launch_pdl("extend_plan_kernel", extend_plan_kernel, dim3(1), dim3(kPlanThreads), 0, s,
+                                extend_lens, prefix_lens, batch, max_extend_len, max_prefix_len, table_stride,
+                                tokens_per_cta, ws.count, ws.items, ws.cap, device_error))
+    return st;
+  // at most sum_b ceil(E_b / tokens_per_cta) entries; CTAs past the listed count return at once
+  const int64_t entries = std::min<int64_t>(ws.cap, static_cast<int64_t>(batch) *
+                                                        ((max_extend_len + tokens_per_cta - 1) / tokens_per_cta));
+  return head_dim == 128 ? launch_extend<128>(p, qmap, entries, s) : launch_extend<64>(p, qmap, entries, s);
+}
+
+extern "C" size_t ra_extend_workspace_bytes(int32_t batch, int64_t total_q, int32_t num_q_heads,
+                                            int32_t num_kv_heads) {
+  if (batch < 0 || total_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads) return 0;
+  const int32_t group = num_q_heads / num_kv_heads;
+  if (128 % group != 0) return 0;
+  return ra::layout_extend_workspace(batch, total_q, ra::tc::kTiles * (128 / group), nullptr).total;
 }

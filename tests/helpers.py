@@ -66,9 +66,12 @@ class DeviceBatch:
         b = self.b
         if b.n_extend == 0:
             return
+        ws = torch.empty(ra.ra_extend_workspace_bytes(b.n_extend, b.total_q_extend, b.num_q_heads, b.num_kv_heads),
+                         dtype=torch.uint8, device=self.dev)
         ra.ra_extend_attention(self.k_pool, self.v_pool, self.ext_q, self.ext_o, self.table, self.ext_rpi,
                                self.ext_prefix, self.ext_len, self.ext_qo, max_extend_len=b.max_extend_len,
-                               max_prefix_len=b.max_prefix_len, sm_scale=b.sm_scale, device_error=self.err)
+                               max_prefix_len=b.max_prefix_len, sm_scale=b.sm_scale, workspace=ws,
+                               device_error=self.err)
 
     def decode_ws(self, cascade: bool) -> torch.Tensor:
         b = self.b

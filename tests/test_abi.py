@@ -27,8 +27,8 @@ def _declared_functions():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    for n in ("ra_kv_store", "ra_extend_attention", "ra_decode_attention", "ra_decode_workspace_bytes",
-              "ra_status_string", "ra_last_error_message", "ra_abi_version"):
+    for n in ("ra_kv_store", "ra_extend_attention", "ra_extend_workspace_bytes", "ra_decode_attention",
+              "ra_decode_workspace_bytes", "ra_status_string", "ra_last_error_message", "ra_abi_version"):
         assert n in names
 
 
@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert ra.ra_abi_version() == 1
+    assert ra.ra_abi_version() == 2
     assert lib.ra_status_string(0) == b"ok"
     assert lib.ra_status_string(3) == b"workspace too small"
 
@@ -80,6 +80,35 @@ def test_decode_workspace_grows_with_bounds(lib):
     d = ra.ra_decode_workspace_bytes(64, 32, 8, 128, 32768)
     assert 0 < b < a < c and d >= a
     assert ra.ra_decode_workspace_bytes(0, 32, 8, 128, 4096) == 0
+
+
+def _extend_call(lib, **over):
+    args = dict(k=FAKE, v=FAKE, S=1024, hkv=8, d=128, q=FAKE, o=FAKE, hq=32, scale=0.088, table=FAKE,
+                stride=4096, rows=64, rpi=FAKE, plen=FAKE, elen=FAKE, qo=FAKE, batch=4, total_q=1000,
+                max_e=500, max_p=3000, ws=FAKE, wsb=16, err=None, stream=None)
+    args.update(over)
+    return lib.ra_extend_attention(*args.values())
+
+
+def test_extend_validation(lib):
+    need = ra.ra_extend_workspace_bytes(4, 1000, 32, 8)
+    assert _extend_call(lib, hq=30) == 1                       # Hq % Hkv != 0
+    assert _extend_call(lib, d=96) == 2                        # unsupported head_dim
+    assert _extend_call(lib, wsb=need - 1) == 3                # workspace too small
+    assert b"workspace" in lib.ra_last_error_message()
+    assert _extend_call(lib, ws=None, wsb=need) == 3           # no workspace
+    assert _extend_call(lib, ws=ctypes.c_void_p((1 << 20) + 4), wsb=need) == 1  # misaligned workspace
+    assert _extend_call(lib, stride=400) == 1                  # table narrower than max_extend_len
+    assert _extend_call(lib, batch=0, ws=None, wsb=0) == 0     # empty batch: no-op, no workspace needed
+    assert _extend_call(lib, total_q=0, ws=None, wsb=0) == 0
+
+
+def test_extend_workspace_bounds_the_work_list(lib):
+    # one (request, query tile) entry per 2 * 128 / G suffix tokens, plus one per request, 8 bytes each
+    assert ra.ra_extend_workspace_bytes(4, 1000, 32, 8) == 16 + 8 * ((1000 + 63) // 64 + 4)
+    assert ra.ra_extend_workspace_bytes(4, 1000, 64, 8) == 16 + 8 * ((1000 + 31) // 32 + 4)
+    assert ra.ra_extend_workspace_bytes(4, 1000, 30, 8) == 0
+    assert ra.ra_extend_workspace_bytes(0, 0, 32, 8) == 16
 
 
 def test_kv_store_validation(lib):
