@@ -40,8 +40,10 @@ namespace {
 constexpr int kSlab = 16;          // keys per ring stage (the MMA M side)
 constexpr int kMaxChunk = 1024;    // keys per item (plan_decode never exceeds it)
 constexpr int kMaxStages = 8;
-constexpr int kItemRing = 16;      // > kMaxStages: an item id is never overwritten before it is read
-constexpr int kHdrBytes = 256 + 2 * kMaxChunk * 4;  // barriers, item ring, flags, 2 slot buffers
+constexpr int kItemRing = 16;      // published items; the leader runs at most nstage + 1 items ahead
+constexpr int kProducers = 4;      // warps issuing the bulk copies of a slab (TMA issue rate grows with them)
+constexpr int kRowsPerProducer = 2 * kSlab / kProducers;  // K rows then V rows of a slab, split evenly
+constexpr int kHdrBytes = 512;     // full/empty barriers, item ring, abort flag, item barriers
 constexpr int kSmemLimit = 227 * 1024;
 
 // One work item: keys [k0, k1) of request b for the kv heads of head group hg.
@@ -77,16 +79,15 @@ __device__ __forceinline__ bool decode_item(const DecodeParams& p, int32_t idx, 
   return true;
 }
 
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-
-// Persistent split-KV decode.  One CTA per SM pulls (request, split, head group) items
-// from a counter.  Warp `hpc` is the producer: per 16-key slab it copies each key's K and
-// V rows of the whole head group (hpc * D * 2 contiguous bytes) with one cp.async.bulk
-// each into a ring stage; consumer warp w owns kv head hg * hpc + w of every item.
+// Persistent split-KV decode.  One CTA per SM pulls (request, split, head group) items from a
+// counter.  Warps hpc .. hpc+3 are producers: per 16-key slab, producer w copies a quarter of the
+// slab's 32 rows -- each key's K row and V row of the whole head group, hpc * D * 2 contiguous bytes
+// -- with one cp.async.bulk each into a ring stage.  The first producer also claims the items and
+// publishes them through a shared ring (with one mbarrier per entry) as soon as it claims them, a
+// few slabs ahead, so every producer looks one slab ahead across items for its slot ids.  Consumer
+// warp w owns kv head hg * hpc + w of every item.
 template <int D>
-__global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + 1), 1) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode_kernel(const DecodeParams p) {
   constexpr int KT = D / 16;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -94,11 +95,11 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + 1), 1) decode_kernel(c
   const int nc = p.hpc;
   const int ns = p.nstage;
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t full0 = sbase;        // ns mbarriers
-  const uint32_t empty0 = sbase + 64;  // ns mbarriers
+  const uint32_t full0 = sbase;        // ns mbarriers (kProducers arrivals + bytes)
+  const uint32_t empty0 = sbase + 64;  // ns mbarriers (nc consumer arrivals)
   volatile int32_t* s_items = reinterpret_cast<volatile int32_t*>(smem + 128);
   volatile int32_t* s_abort = reinterpret_cast<volatile int32_t*>(smem + 192);
-  int32_t* s_slots = reinterpret_cast<int32_t*>(smem + 256);
+  const uint32_t item0 = sbase + 256;  // kItemRing mbarriers: entry published
   const uint32_t stage0 = sbase + kHdrBytes;
   const int RS = p.row_stride;
   // Let the combine launch; this kernel reads nothing its predecessor (the cascade prefix pass, which
@@ -107,18 +108,26 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + 1), 1) decode_kernel(c
   griddep_launch();
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s) {
-      mbar_init(full0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, kProducers);
       mbar_init(empty0 + 8 * s, nc);
     }
+    for (int s = 0; s < kItemRing; ++s) mbar_init(item0 + 8 * s, 1);
     *s_abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
   const int row_bytes = p.hpc * D * 2;
 
-  if (warp == nc) {
-    // ================================================================ producer
-    auto claim = [&]() -> int32_t {
+  if (warp >= nc && warp < nc + kProducers) {
+    // ================================================================ producers
+    const int pw = warp - nc;
+    const bool leader = pw == 0;
+    const int row_id = pw * kRowsPerProducer + lane;  // this lane's row of a slab (lane < kRowsPerProducer)
+    const bool is_v = row_id >= kSlab;
+    const int key_in_slab = row_id & (kSlab - 1);
+    const __nv_bfloat16* pool = is_v ? p.v_pool : p.k_pool;
+    const uint32_t row_off = (is_v ? kSlab * RS : 0) + key_in_slab * RS;
+    auto claim = [&]() -> int32_t {  // warp-collective
       for (;;) {
         int32_t idx = 0;
         if (lane == 0) idx = atomicAdd(p.counter, 1);
@@ -131,65 +140,79 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + 1), 1) decode_kernel(c
         if (lane == 0) atomicMax(p.counter, (idx / per_req + 1) * per_req);
       }
     };
-    auto prefetch = [&](int32_t idx, int buf) {  // the item's slot ids -> s_slots[buf]
-      Item it;
-      decode_item(p, idx, it, false);
-      const int32_t* rp = p.table + static_cast<int64_t>(it.row) * p.table_stride + it.k0;
-      for (int k = lane; k < it.k1 - it.k0; k += 32) cp_async4(smem_u32(s_slots + buf * kMaxChunk + k), rp + k);
-      asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-    int32_t n = 0, c = 0, buf = 0;
-    int32_t cur = claim();
-    if (cur >= 0) prefetch(cur, 0);
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    __syncwarp();
-    bool ok = true;
-    while (cur >= 0) {
-      Item it;
-      decode_item(p, cur, it, false);
-      const int32_t nk = it.k1 - it.k0;
-      const int32_t n_slabs = (nk + kSlab - 1) / kSlab;
-      // claim the next item once this one's first stages are issued (its latency then overlaps)
-      const int32_t claim_at = (n_slabs < ns ? n_slabs : ns) - 1;
-      int32_t nxt = -1;
-      const __nv_bfloat16* base = (lane < 16 ? p.k_pool : p.v_pool) + static_cast<int64_t>(it.hg) * p.hpc * D;
-      for (int32_t s = 0; s < n_slabs; ++s, ++c) {
-        const int st = c % ns;
-        if (c >= ns && !mbar_wait(empty0 + 8 * st, ((c / ns) + 1) & 1)) { ok = false; break; }
-        if (*s_abort) { ok = false; break; }
-        if (s == 0 && lane == 0) s_items[n % kItemRing] = cur;
-        if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, 2 * kSlab * row_bytes);
-        __syncwarp();
-        int32_t key = s * kSlab + (lane & 15);
-        key = key < nk ? key : nk - 1;  // rows past the range repeat the last key (finite, weight 0)
-        int32_t slot = s_slots[buf * kMaxChunk + key];
-        if (slot < 0 || slot >= p.num_slots) {
-          flag_error(p.err, RA_DEVERR_SLOT);
-          slot = 0;
-        }
-        const uint32_t dst = stage0 + st * p.stage_bytes + (lane < 16 ? 0 : kSlab * RS) + (lane & 15) * RS;
-        bulk_g2s(dst, base + static_cast<int64_t>(slot) * p.hkv * D, row_bytes, full0 + 8 * st);
-        if (s == claim_at) {
-          nxt = claim();
-          if (nxt >= 0) prefetch(nxt, buf ^ 1);
-        }
+    auto publish = [&](int32_t n, int32_t idx) {
+      if (lane == 0) {
+        s_items[n % kItemRing] = idx;
+        mbar_arrive(item0 + 8 * (n % kItemRing));
       }
-      if (!ok) break;
-      asm volatile("cp.async.wait_group 0;" ::: "memory");  // the next item's slot ids
+    };
+    // 1: item n in `it`; 0: end of work; -1: a bounded wait ran out
+    auto next_item = [&](int32_t n, Item& it) -> int {
+      if (!mbar_wait(item0 + 8 * (n % kItemRing), (n / kItemRing) & 1)) return -1;
+      const int32_t idx = s_items[n % kItemRing];
+      if (idx < 0) return 0;
+      decode_item(p, idx, it, false);
+      return 1;
+    };
+    auto load_slot = [&](const Item& it, int32_t s) -> int32_t {  // rows past the range repeat the last key
+      if (lane >= kRowsPerProducer) return 0;
+      const int32_t nk = it.k1 - it.k0;
+      int32_t key = s * kSlab + key_in_slab;
+      key = key < nk ? key : nk - 1;
+      return __ldg(p.table + static_cast<int64_t>(it.row) * p.table_stride + it.k0 + key);
+    };
+    if (leader) publish(0, claim());
+    int32_t n = 0, c = 0, s = 0;
+    Item it;
+    int r = next_item(0, it);
+    bool ok = r >= 0;
+    int32_t slot = r > 0 ? load_slot(it, 0) : 0;
+    while (ok && r > 0) {
+      const int32_t n_slabs = (it.k1 - it.k0 + kSlab - 1) / kSlab;
+      // the leader claims the next item when this one has ns slabs left to issue: the claim overlaps
+      // them, and items stay unclaimed for CTAs that start late (behind a cascade prefix pass that
+      // holds their SMs) instead of queueing behind this one
+      if (leader && s == (n_slabs > ns ? n_slabs - ns : 0)) publish(n + 1, claim());
+      // one slab ahead: the next (item, slab) and its slot id
+      Item it2 = it;
+      int32_t s2 = s + 1, n2 = n;
+      int r2 = 1;
+      if (s2 == n_slabs) {
+        n2 = n + 1;
+        s2 = 0;
+        r2 = next_item(n2, it2);
+        if (r2 < 0) { ok = false; break; }
+      }
+      const int32_t slot2 = r2 > 0 ? load_slot(it2, s2) : 0;
+      // slab s of item n into stage c % ns
+      const int st = c % ns;
+      if (c >= ns && !mbar_wait(empty0 + 8 * st, ((c / ns) + 1) & 1)) { ok = false; break; }
+      if (*s_abort) { ok = false; break; }
+      if (lane == 0) mbar_arrive_expect_tx(full0 + 8 * st, kRowsPerProducer * row_bytes);
       __syncwarp();
-      ++n;
-      cur = nxt;
-      buf ^= 1;
+      if (lane < kRowsPerProducer) {
+        int32_t sl = slot;
+        if (sl < 0 || sl >= p.num_slots) {
+          flag_error(p.err, RA_DEVERR_SLOT);
+          sl = 0;
+        }
+        bulk_g2s(stage0 + st * p.stage_bytes + row_off,
+                 pool + static_cast<int64_t>(sl) * p.hkv * D + static_cast<int64_t>(it.hg) * p.hpc * D, row_bytes,
+                 full0 + 8 * st);
+      }
+      ++c;
+      it = it2;
+      s = s2;
+      n = n2;
+      r = r2;
+      slot = slot2;
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
     if (ok) {
-      // end marker: item id -1 published through the next stage
+      // end of work (entry n holds -1): every producer arrives on the next stage, the consumers read
+      // the marker from it
       const int st = c % ns;
       if (c >= ns && !mbar_wait(empty0 + 8 * st, ((c / ns) + 1) & 1)) ok = false;
-      if (ok && lane == 0) {
-        s_items[n % kItemRing] = -1;
-        mbar_arrive(full0 + 8 * st);
-      }
+      if (ok && lane == 0) mbar_arrive(full0 + 8 * st);
     }
     if (!ok) {
       if (lane == 0) {
@@ -202,7 +225,7 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + 1), 1) decode_kernel(c
     griddep_wait();
     return;
   }
-  if (warp > nc) {
+  if (warp >= nc + kProducers) {
     griddep_wait();
     return;
   }
@@ -443,7 +466,8 @@ ra_status launch_decode(const DecodeParams& p, int grid, int smem, cudaStream_t 
     if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaFuncSetAttribute(decode): %s", cudaGetErrorString(e));
     configured[dev.device] = kSmemLimit;
   }
-  if (ra_status st = launch_pdl("decode_kernel", kern, dim3(grid), dim3(32 * (p.hpc + 1)), smem, stream, p)) return st;
+  if (ra_status st = launch_pdl("decode_kernel", kern, dim3(grid), dim3(32 * (p.hpc + kProducers)), smem, stream, p))
+    return st;
   const int nwarps = p.batch * p.hq;
   return launch_pdl("decode_combine_kernel", decode_combine_kernel<D>, dim3((nwarps + 3) / 4), dim3(128), 0, stream, p);
 }
@@ -475,18 +499,31 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
   pl.max_splits = static_cast<int32_t>((static_cast<int64_t>(max_seq_len) + chunk - 1) / chunk);
   if (pl.max_splits < 1) pl.max_splits = 1;
   if (num_groups > 0 && max_group_prefix_len > 0) {
-    // prefix keys per prefix-pass CTA: split so that about 96 CTAs exist (the rest of the SMs run the
-    // private decode meanwhile), but no CTA covers more than 2048 prefix keys; a multiple of the 128-key tile
+    // Prefix keys per prefix-pass CTA (a multiple of the 128-key tile, at most 2048): the split count
+    // that minimises the pass's makespan, waves x (tiles per CTA + the ~3 tiles' worth of fill and
+    // drain a CTA costs), one CTA per SM; on a tie the fewer CTAs.
     const int32_t group = num_q_heads / num_kv_heads;
     const int64_t members_per_cta = 2 * (128 / (group > 0 ? group : 1));  // two 128-row query tiles
     const int64_t mtiles = (max_group_size + members_per_cta - 1) / members_per_cta;
     const int64_t base = static_cast<int64_t>(num_groups) * num_kv_heads * mtiles;
-    const int64_t want = (96 + base - 1) / base;
-    int64_t cchunk = (max_group_prefix_len + want - 1) / want;
-    cchunk = (cchunk + 127) / 128 * 128;
-    if (cchunk > 2048) cchunk = 2048;
-    pl.cchunk = static_cast<int32_t>(cchunk);
-    pl.max_csplits = static_cast<int32_t>((max_group_prefix_len + cchunk - 1) / cchunk);
+    const int64_t tiles = (max_group_prefix_len + 127) / 128;
+    // CTAs per wave: two thirds of GB300's 152 SMs, the rest run the private decode beside the pass.
+    // A constant: the workspace size (sized on the host, possibly with no device current) must not
+    // depend on which device runs the call; only the split balance does.
+    constexpr int64_t sms = 104;
+    int64_t best_tiles = 16, best_cost = -1;
+    for (int64_t per = 16; per >= 1; --per) {  // tiles per CTA
+      const int64_t splits = (tiles + per - 1) / per;
+      const int64_t waves = (base * splits + sms - 1) / sms;
+      const int64_t cost = waves * (per + 3);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best_tiles = per;
+      }
+    }
+    if (best_tiles > tiles) best_tiles = tiles;
+    pl.cchunk = static_cast<int32_t>(best_tiles * 128);
+    pl.max_csplits = static_cast<int32_t>((max_group_prefix_len + pl.cchunk - 1) / pl.cchunk);
   }
   return pl;
 }

@@ -139,3 +139,17 @@ def grow_key_scale(b: W.Batch, per_tile: float = 6.0, tile: int = 128) -> W.Batc
     b.pool_k = scaled(b.pool_k, b.pool_slots)
     b.k_new = scaled(b.k_new, b.out_cache_loc)
     return b
+
+
+def prefill_chunks(b: W.Batch, chunk: int):
+    """Chunked prefill of an extend batch: call k extends every request by its k-th chunk of at most
+    `chunk` suffix tokens, with all earlier chunks as cached prefix.  Yields, per call, (q rows,
+    prefix_lens, extend_lens, qo_indptr, token index of each row in the unchunked batch)."""
+    P, E, qo = b.ext_prefix_lens, b.ext_extend_lens, b.ext_qo_indptr
+    n_calls = int(-(-E.max() // chunk))
+    for k in range(n_calls):
+        done = np.minimum(k * chunk, E)
+        ext = np.minimum(chunk, E - done).astype(np.int32)
+        toks = np.concatenate([qo[i] + done[i] + np.arange(ext[i]) for i in range(E.size)]).astype(np.int64)
+        yield (b.ext_q[toks], (P + done).astype(np.int32), ext,
+               np.concatenate([[0], np.cumsum(ext)]).astype(np.int32), toks)

@@ -7,7 +7,7 @@ import torch
 import oracle
 import prefix_shared_kv_ra_gb300 as ra
 import workloads as W
-from helpers import DeviceBatch, assert_close, attach_tree_groups, grow_key_scale, to_f64
+from helpers import DeviceBatch, assert_close, attach_tree_groups, grow_key_scale, prefill_chunks, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -60,6 +60,35 @@ def test_extend_growing_scores(seed, hq, hkv, d):
     db = DeviceBatch(b)
     db.store()
     check_extend(db)
+
+
+@pytest.mark.parametrize("chunk", [64, 100])
+def test_chunked_prefill(chunk):
+    """Chunked prefill through the C ABI: each call extends every request by one chunk over its
+    cached prefix plus the chunks before it; the rows equal the oracle's single extend."""
+    b = W.random_mixed(24, n_extend=6, n_decode=0, num_q_heads=32, num_kv_heads=8, head_dim=128, max_len=600,
+                       min_len=200)
+    db = DeviceBatch(b)
+    db.store()
+    db.extend()
+    full_gpu = to_f64(db.ext_o).reshape(b.total_q_extend, b.num_q_heads, b.head_dim)
+    ref = oracle.extend_batch(b).reshape(b.total_q_extend, b.num_q_heads, b.head_dim)
+    dev = db.dev
+    got = np.zeros_like(ref)
+    for q, plen, elen, qo, toks in prefill_chunks(b, chunk):
+        qd = torch.from_numpy(q.view(np.int16)).to(dev).view(torch.bfloat16)
+        od = torch.empty_like(qd)
+        ws = torch.empty(ra.ra_extend_workspace_bytes(b.n_extend, qd.shape[0], b.num_q_heads, b.num_kv_heads),
+                         dtype=torch.uint8, device=dev)
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+        ra.ra_extend_attention(db.k_pool, db.v_pool, qd, od, db.table, db.ext_rpi, i32(plen), i32(elen), i32(qo),
+                               max_extend_len=chunk, max_prefix_len=int(plen.max()), sm_scale=b.sm_scale,
+                               workspace=ws, device_error=db.err)
+        torch.cuda.synchronize()
+        got[toks] = to_f64(od).reshape(-1, b.num_q_heads, b.head_dim)
+    assert int(db.err.item()) == 0
+    assert_close(got.reshape(-1, b.head_dim), ref.reshape(-1, b.head_dim), "chunked prefill vs oracle")
+    assert_close(got.reshape(-1, b.head_dim), full_gpu.reshape(-1, b.head_dim), "chunked vs one extend")
 
 
 def test_extend_fewshot_full():

@@ -144,6 +144,23 @@ def test_prefix_reuse_equals_full_attention_on_fresh_pool():
         np.testing.assert_allclose(mine, full[P * 4:], rtol=0, atol=1e-13)
 
 
+def test_chunked_prefill_equals_one_extend():
+    """Prefilling a suffix in chunks, each chunk attending to the cached prefix plus the earlier
+    chunks, gives the rows of one extend over the whole suffix (the KV of a position depends only
+    on the tokens before it, SGLang paper summary §3)."""
+    from helpers import prefill_chunks
+    b = W.random_mixed(23, n_extend=5, n_decode=0, num_q_heads=8, num_kv_heads=2, head_dim=16, max_len=90,
+                       share_prob=0.7)
+    full = oracle.extend_batch(b).reshape(-1, b.num_q_heads, b.head_dim)
+    pool = oracle.pool_after_store(b)
+    seen = np.zeros(b.total_q_extend, bool)
+    for q, plen, elen, qo, toks in prefill_chunks(b, 13):
+        part = oracle.extend(pool, q, b.req_to_token, b.ext_rpi, plen, elen, qo, b.sm_scale)
+        np.testing.assert_allclose(part.reshape(-1, b.num_q_heads, b.head_dim), full[toks], rtol=0, atol=1e-13)
+        seen[toks] = True
+    assert seen.all()
+
+
 def test_slot_permutation_invariance():
     b = W.random_mixed(31, n_extend=3, n_decode=5, num_q_heads=8, num_kv_heads=2, head_dim=8, max_len=40)
     oe, od = oracle.extend_batch(b), oracle.decode_batch(b)
