@@ -483,9 +483,9 @@ static int32_t heads_per_cta(int32_t num_kv_heads) {
 
 // Private keys per work item: between 256 and 1024, aiming at ~1K (request, split, head group)
 // items over the host-side bound of the batch's keys.
-// Shared-prefix pass (cascade): 256-row tiles of (member, q head) per group and kv head; each CTA covers
-// at most `cchunk` prefix keys (about 96 CTAs, at most 2048 keys each).  The persistent private decode is
-// launched programmatically after it and runs on the SMs the prefix pass leaves free.
+// Shared-prefix pass (cascade): 256-row items of (member, q head) per group and kv head, each covering
+// at most `cchunk` prefix keys.  The persistent private decode is launched programmatically after it
+// and runs on the SMs the prefix pass leaves free.
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seq_len,
                        int32_t num_groups, int32_t max_group_prefix_len, int32_t max_group_size) {
   DecodePlan pl;
@@ -546,7 +546,7 @@ DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int3
   }
   w.ints = off;
   (void)num_kv_heads;
-  w.ints_bytes = (static_cast<size_t>(batch) + 1) * sizeof(int32_t);
+  w.ints_bytes = (static_cast<size_t>(batch) + 2) * sizeof(int32_t);
   off += up(w.ints_bytes);
   w.total = off;
   return w;
@@ -635,6 +635,7 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
 
   int32_t* ints = reinterpret_cast<int32_t*>(ws + wl.ints);
   p.counter = ints + batch;
+  p.prefix_counter = ints + batch + 1;
   cudaError_t e = cudaMemsetAsync(ints, 0, wl.ints_bytes, s);
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
   if (num_groups > 0) {

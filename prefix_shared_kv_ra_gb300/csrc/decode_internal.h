@@ -40,6 +40,7 @@ struct DecodeParams {
   int32_t stage_bytes;       // 2 * 16 * row_stride
   int32_t n_items;           // max_splits * batch * n_hgroups
   int32_t* counter;          // work-item counter (zeroed before each launch)
+  int32_t* prefix_counter;   // cascade prefix pass's work-item counter (zeroed likewise)
   float* part_o;    // [batch, hq, max_splits, D]
   float* part_lse;  // [batch, hq, max_splits] (log2 domain)
   int32_t cchunk;      // shared-prefix keys per prefix-pass split (cascade)
@@ -58,7 +59,7 @@ struct DecodePlan {
 
 struct DecodeWorkspace {
   size_t part_o = 0, part_lse = 0, casc_o = 0, casc_lse = 0;
-  size_t ints = 0, ints_bytes = 0;  // one zeroed block: key_start [batch], counter [1]
+  size_t ints = 0, ints_bytes = 0;  // one zeroed block: key_start [batch], counter, prefix counter
   size_t total = 0;
 };
 

@@ -34,8 +34,9 @@ constexpr int kPlanThreads = 1024;
 constexpr int kPlanBins = 4096;  // key-tile counts above kPlanBins - 1 share the first bin
 
 struct ExtendWorkspace {
-  int32_t* count;  // entries listed
-  int32_t* items;  // [2 * cap]
+  int32_t* count;    // entries listed
+  int32_t* counter;  // item claim counter of the persistent kernel
+  int32_t* items;    // [2 * cap]
   int64_t cap;
   size_t total;
 };
@@ -47,6 +48,7 @@ ExtendWorkspace layout_extend_workspace(int32_t batch, int64_t total_q, int32_t 
   w.total = 16 + static_cast<size_t>(w.cap) * 8;
   uint8_t* b = static_cast<uint8_t*>(base);
   w.count = reinterpret_cast<int32_t*>(b);
+  w.counter = reinterpret_cast<int32_t*>(b ? b + 4 : nullptr);
   w.items = reinterpret_cast<int32_t*>(b ? b + 16 : nullptr);
   return w;
 }
@@ -61,8 +63,8 @@ __global__ void __launch_bounds__(kPlanThreads) extend_plan_kernel(const int32_t
                                                                   const int32_t* prefix_lens, int32_t batch,
                                                                   int32_t max_extend_len, int32_t max_prefix_len,
                                                                   int64_t table_stride, int32_t tokens_per_cta,
-                                                                  int32_t* count, int32_t* items, int64_t cap,
-                                                                  uint32_t* err) {
+                                                                  int32_t* count, int32_t* counter, int32_t* items,
+                                                                  int64_t cap, uint32_t* err) {
   __shared__ int32_t s_bin[kPlanBins];
   __shared__ int32_t s_warp[kPlanThreads / 32];
   griddep_launch();  // the extend kernel may start its launch; it waits for this grid before reading the list
@@ -134,7 +136,10 @@ __global__ void __launch_bounds__(kPlanThreads) extend_plan_kernel(const int32_t
       }
     }
   }
-  if (threadIdx.x == 0) *count = static_cast<int32_t>(static_cast<int64_t>(total) < cap ? total : cap);
+  if (threadIdx.x == 0) {
+    *count = static_cast<int32_t>(static_cast<int64_t>(total) < cap ? total : cap);
+    *counter = 0;
+  }
   griddep_wait();  // complete only after the previous grid (the KV store): the extend kernel waits on this one
 }
 
@@ -206,7 +211,9 @@ ra_status launch_extend(const TcParams& p, const CUtensorMap& qmap, int64_t entr
   if (L::kDynSmem > dev.max_smem_optin)
     return fail(RA_ERR_UNSUPPORTED, "extend kernel needs %d bytes of shared memory", L::kDynSmem);
   if (ra_status st = set_smem(kern, L::kDynSmem, configured, dev.device)) return st;
-  dim3 grid(static_cast<unsigned>(entries * p.hkv));
+  // persistent: one CTA per SM (at most one per item)
+  const int64_t items = entries * p.hkv;
+  dim3 grid(static_cast<unsigned>(items < dev.num_sms ? items : dev.num_sms));
   return launch_pdl("attn_tc_kernel<extend>", kern, grid, dim3(tc::kThreads), L::kDynSmem, s, p, qmap, kmap, vmap);
 }
 
@@ -224,7 +231,9 @@ ra_status launch_prefix(const TcParams& p, int grid_x, int num_groups, cudaStrea
   if (ra_status st = row_gather_map(&qmap, p.q, static_cast<int64_t>(p.batch) * p.hq, D)) return st;
   if (ra_status st = row_gather_map(&kmap, p.k_pool, p.num_slots * p.hkv, D)) return st;
   if (ra_status st = row_gather_map(&vmap, p.v_pool, p.num_slots * p.hkv, D)) return st;
-  dim3 grid(grid_x, p.hkv, num_groups);
+  // persistent: one CTA per SM (at most one per item)
+  const int64_t items = static_cast<int64_t>(grid_x) * p.hkv * num_groups;
+  dim3 grid(static_cast<unsigned>(items < dev.num_sms ? items : dev.num_sms));
   return launch_pdl("attn_tc_kernel<cascade prefix>", kern, grid, dim3(tc::kThreads), L::kDynSmem, s, p, qmap, kmap,
                     vmap);
 }
@@ -258,9 +267,12 @@ ra_status launch_cascade_prefix(const DecodeParams& d, const CascadeArgs& ca, in
   p.max_csplits = d.max_csplits;
   p.casc_o = d.casc_o;
   p.casc_lse = d.casc_lse;
+  p.work_counter = d.prefix_counter;
+  p.num_groups = ca.num_groups;
   const int members_per_cta = tc::kTiles * (128 / d.group);
   const int mtiles = (ca.max_group_size + members_per_cta - 1) / members_per_cta;
   const int grid_x = mtiles * d.max_csplits;
+  p.grid_x = grid_x;
   return head_dim == 128 ? launch_prefix<128>(p, grid_x, ca.num_groups, stream)
                          : launch_prefix<64>(p, grid_x, ca.num_groups, stream);
 }
@@ -345,11 +357,12 @@ extern "C" ra_status ra_extend_attention(const void* k_pool, const void* v_pool,
   p.max_prefix_len = max_prefix_len;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.work_count = ws.count;
+  p.work_counter = ws.counter;
   p.work_items = ws.items;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (ra_status st = launch_pdl("extend_plan_kernel", extend_plan_kernel, dim3(1), dim3(kPlanThreads), 0, s,
                                 extend_lens, prefix_lens, batch, max_extend_len, max_prefix_len, table_stride,
-                                tokens_per_cta, ws.count, ws.items, ws.cap, device_error))
+                                tokens_per_cta, ws.count, ws.counter, ws.items, ws.cap, device_error))
     return st;
   // at most sum_b ceil(E_b / tokens_per_cta) entries; CTAs past the listed count return at once
   const int64_t entries = std::min<int64_t>(ws.cap, static_cast<int64_t>(batch) *
