@@ -442,6 +442,20 @@ def run_profile_case(name: str, steps: int):
                       "device_error": int(st.err.item())}))
 
 
+# ----------------------------------------------------------------------------- ranks
+def reduce_over_ranks(dist, device, step_ms: float, e2e_ms: float, tokens: int):
+    """Whole-job figures of independent replicas: the slowest rank's step and end-to-end times and the
+    tokens all ranks processed (each rank draws its own batch).  dist None = one process."""
+    if dist is None:
+        return step_ms, e2e_ms, tokens
+    import torch
+    t = torch.tensor([step_ms, e2e_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor([tokens], dtype=torch.int64, device=device)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t[0].item()), float(t[1].item()), int(n.item())
+
+
 # ----------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -501,18 +515,11 @@ def main():
     r = time_steps(step, args.steps, args.warmup, flush, sample_clocks_uuid=uuid)
     step_ms = float(np.mean(r["step_ms"]))
     if dist:
-        t = torch.tensor([step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t.item())
         dist.barrier()
-    tokens = b.total_q_extend + b.n_decode
-    value = tokens * world / step_ms * 1e3
-
     e2e_ms, h2d, d2h = e2e_steps(step, args.steps, args.warmup, flush)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    tokens = b.total_q_extend + b.n_decode
+    step_ms, e2e_ms, job_tokens = reduce_over_ranks(dist, dev, step_ms, e2e_ms, tokens)
+    value = job_tokens / step_ms * 1e3
     if rank != 0:
         dist.barrier()
         dist.destroy_process_group()
@@ -544,7 +551,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "global_batch": 256 * world, "tokens_per_step": tokens * world,
+        "config": {"workload": WORKLOAD, "global_batch": 256 * world, "tokens_per_step": job_tokens,
                    "extend_tokens": b.total_q_extend, "decode_tokens": b.n_decode, "l2": "flushed (256 MB write)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "hit_ratio": round(b.meta["construction_hit_ratio"], 4)},
@@ -560,7 +567,7 @@ def main():
             "other_workloads": extra,
         },
         "cpu_baseline": {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
-        "e2e": {"value": tokens * world / e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_tokens / e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches * args.steps,
         "source_digest": source_digest(),
