@@ -326,6 +326,7 @@ def extra_kernels(dev, flush, peaks, reps: int = 20):
     import workloads as W
     out = {}
     specs = [("decode_8b_system_prompts", W.cfg2_decode_8b, (False, True)),
+             ("decode_8b_system_prompts_page16", lambda: W.cfg2_decode_8b(page_size=16), (False,)),
              ("extend_fewshot_3000", W.cfg3_fewshot_extend, (False,)),
              ("decode_70b_forked_8192", W.cfg4_forked_decode_70b, (False, True))]
     for name, fn, modes in specs:

@@ -12,7 +12,10 @@ RadixAttention"; the yaopepe.com explainer, §04):
 * running requests hold a reference on every node of their path; only
   unreferenced leaves may be evicted, least recently used first, and a parent
   that becomes an unreferenced leaf becomes a candidate in turn;
-* evicted slots go back to the slot pool for reuse.
+* evicted slots go back to the slot pool for reuse;
+* with pages of P > 1 slots (P consecutive slots per page), the cache shares
+  whole pages only: matches and inserts are cut to a multiple of P, so every
+  edge starts and ends on a page boundary and eviction frees whole pages.
 
 This is support code for the attention path: it produces the
 ``req_to_token`` rows, the cascade groups and the hit ratio the kernels and
@@ -30,26 +33,37 @@ __all__ = ["SlotPool", "RadixCache", "cascade_groups"]
 
 
 class SlotPool:
-    """Free list of token slots [1, num_slots); slot 0 is the dummy slot padded requests write."""
+    """Free list of token slots in pages of `page_size` consecutive slots; page 0 (holding slot 0,
+    the dummy slot padded requests write) is never handed out."""
 
-    def __init__(self, num_slots: int):
+    def __init__(self, num_slots: int, page_size: int = 1):
+        if page_size < 1 or num_slots % page_size:
+            raise ValueError("num_slots must be a multiple of page_size")
         self.num_slots = int(num_slots)
-        self._free = list(range(self.num_slots - 1, 0, -1))  # pop() hands out low slots first
+        self.page_size = int(page_size)
+        self._free = list(range(self.num_slots // page_size - 1, 0, -1))  # free pages; pop() gives low ones first
 
     def available(self) -> int:
-        return len(self._free)
+        """Free slots (whole pages)."""
+        return len(self._free) * self.page_size
 
     def alloc(self, n: int) -> Optional[np.ndarray]:
-        if n > len(self._free):
+        """Slots for n new tokens, in order: the first n slots of ceil(n / page_size) fresh pages (the rest
+        of the last page stays with the caller until freed)."""
+        pages = -(-n // self.page_size)
+        if pages > len(self._free):
             return None
-        out = [self._free.pop() for _ in range(n)]
-        return np.asarray(out, dtype=np.int32)
+        out = np.asarray([self._free.pop() for _ in range(pages)], dtype=np.int64)
+        slots = (out[:, None] * self.page_size + np.arange(self.page_size)[None, :]).reshape(-1)[:n]
+        return slots.astype(np.int32)
 
     def free(self, slots: Sequence[int]) -> None:
-        for s in np.asarray(slots, dtype=np.int64).tolist():
-            if not 1 <= s < self.num_slots:
-                raise ValueError(f"slot {s} out of range")
-            self._free.append(int(s))
+        """Return the pages holding these slots."""
+        s = np.asarray(slots, dtype=np.int64)
+        if s.size and (s.min() < self.page_size or s.max() >= self.num_slots):
+            raise ValueError("slot out of range")
+        for pg in np.unique(s // self.page_size).tolist():
+            self._free.append(int(pg))
 
 
 class _Node:
@@ -77,6 +91,7 @@ def _common_len(a: np.ndarray, b: np.ndarray) -> int:
 class RadixCache:
     def __init__(self, pool: SlotPool):
         self.pool = pool
+        self.page = pool.page_size
         self.root = _Node(np.zeros(0, np.int32), np.zeros(0, np.int32), None)
         self.root.lock_ref = 1  # never evicted
         self._clock = 0
@@ -87,7 +102,7 @@ class RadixCache:
         return self._clock
 
     def match_prefix(self, tokens: Sequence[int]) -> Tuple[np.ndarray, _Node]:
-        """Slots of the longest cached prefix of `tokens` and the node where it ends
+        """Slots of the longest cached prefix of `tokens` (whole pages) and the node where it ends
         (an edge matched part-way is split there)."""
         key = np.asarray(tokens, dtype=np.int32)
         node, pos, slots = self.root, 0, []
@@ -97,8 +112,10 @@ class RadixCache:
             child = node.children.get(int(key[pos]))
             if child is None:
                 break
+            k = _common_len(child.key, key[pos:]) // self.page * self.page
+            if k == 0:
+                break
             child.last_access = now
-            k = _common_len(child.key, key[pos:])
             if k < child.key.size:
                 child = self._split(child, k)
                 slots.append(child.value)
@@ -124,11 +141,13 @@ class RadixCache:
         return mid
 
     def insert(self, tokens: Sequence[int], slots: Sequence[int]) -> int:
-        """Insert tokens with their slots; returns how many leading tokens were already cached
-        (the caller frees its duplicate slots for those positions)."""
+        """Insert tokens with their slots (their whole pages only); returns how many leading tokens
+        were already cached (the caller frees its duplicate slots for those positions)."""
         key = np.asarray(tokens, dtype=np.int32)
         val = np.asarray(slots, dtype=np.int32)
         assert key.size == val.size
+        n = key.size // self.page * self.page
+        key, val = key[:n], val[:n]
         matched, node = self.match_prefix(key)
         k = matched.size
         if k < key.size:

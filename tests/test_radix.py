@@ -99,3 +99,49 @@ def test_cascade_groups_share_their_prefix_slots():
             np.testing.assert_array_equal(rows[m][:gp[g]], lead)
         # the group prefix is the shortest member's context minus its own new token, at most the prompt
         assert gp[g] == min(1024, min(rows[m].size - 1 for m in mem))
+
+
+def test_paged_pool_hands_out_whole_pages_in_order():
+    pool = SlotPool(64, page_size=16)
+    assert pool.available() == 48  # page 0 (slots 0-15, the padding slot's page) is reserved
+    a = pool.alloc(20)
+    assert a.size == 20 and np.array_equal(a[:16], np.arange(16, 32)) and np.array_equal(a[16:], np.arange(32, 36))
+    assert pool.available() == 16 and pool.alloc(17) is None
+    pool.free(a)
+    assert pool.available() == 48
+
+
+def test_paged_cache_shares_whole_pages_only():
+    P = 4
+    pool = SlotPool(256, page_size=P)
+    cache = RadixCache(pool)
+    seq = list(range(100, 114))                      # 14 tokens: 3 whole pages cached
+    slots = pool.alloc(len(seq))
+    assert cache.insert(seq, slots) == 0
+    assert cache.total_tokens() == 12
+    got, _ = cache.match_prefix(seq)
+    assert np.array_equal(got, slots[:12])
+    other = seq[:9] + [7, 7, 7]                      # shares 9 tokens: 2 whole pages
+    got, node = cache.match_prefix(other)
+    assert got.size == 8 and np.array_equal(got, slots[:8])
+    assert all(len(e) % P == 0 for _, e in cache.edges())  # the split fell on a page boundary
+    assert cache.match_prefix(seq[:3])[0].size == 0        # less than a page: no hit
+
+
+def test_paged_eviction_frees_whole_pages():
+    P = 8
+    pool = SlotPool(128, page_size=P)
+    cache = RadixCache(pool)
+    a = list(range(32))
+    b = a[:16] + list(range(500, 516))
+    sa = pool.alloc(32)
+    cache.insert(a, sa)
+    hit, _ = cache.match_prefix(b)
+    assert hit.size == 16
+    sb = np.concatenate([hit, pool.alloc(16)])
+    cache.insert(b, sb)
+    free0 = pool.available()
+    assert cache.evict(1) == 16                      # one whole leaf (two pages)
+    assert pool.available() == free0 + 16
+    assert cache.evict(100) == 32                    # the other leaf, then the shared parent
+    assert pool.available() == 120

@@ -169,11 +169,14 @@ def build_batch(name: str, specs: Sequence[SeqSpec], *, num_slots: int, num_q_he
                 num_kv_heads: int, head_dim: int, seed: int,
                 cascade: Optional[Sequence[Tuple[Sequence[int], int]]] = None,
                 spare_rows: int = 3, sm_scale: Optional[float] = None,
-                meta: Optional[Dict] = None) -> Batch:
+                meta: Optional[Dict] = None, page_size: int = 1) -> Batch:
     """Assign slots and draw values for ``specs``.
 
     ``cascade``: optional list of (spec indices of decode members, prefix_len);
     the first member is the group leader whose table row holds the prefix.
+    ``page_size`` > 1: slots come in pages of that many consecutive slots (page 0
+    reserved); a sequence's own tokens fill fresh pages in order, and sharing
+    with a parent is page-granular (every fork a multiple of the page size).
     """
     specs = list(specs)
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -191,8 +194,23 @@ def build_batch(name: str, specs: Sequence[SeqSpec], *, num_slots: int, num_q_he
             assert s.fork == 0, s
 
     n_unique = sum(s.total_len - s.fork for s in specs)
-    assert n_unique <= num_slots - 1, (n_unique, num_slots)
-    fresh = (rng.permutation(num_slots - 1)[:n_unique] + 1).astype(np.int32)
+    if page_size == 1:
+        assert n_unique <= num_slots - 1, (n_unique, num_slots)
+        fresh = (rng.permutation(num_slots - 1)[:n_unique] + 1).astype(np.int32)
+    else:
+        assert page_size > 1 and num_slots % page_size == 0, (page_size, num_slots)
+        assert all(s.fork % page_size == 0 for s in specs), "forks must be page-aligned"
+        n_pages = sum(-(-(s.total_len - s.fork) // page_size) for s in specs)
+        assert n_pages <= num_slots // page_size - 1, (n_pages, num_slots // page_size)
+        pages = rng.permutation(num_slots // page_size - 1)[:n_pages] + 1
+        runs, k = [], 0
+        for s in specs:  # each sequence's own tokens: its pages' slots in order
+            own = s.total_len - s.fork
+            npg = -(-own // page_size)
+            pg = pages[k:k + npg]
+            k += npg
+            runs.append((pg[:, None] * page_size + np.arange(page_size)[None, :]).reshape(-1)[:own])
+        fresh = (np.concatenate(runs) if runs else np.zeros(0, np.int64)).astype(np.int32)
 
     slots: List[np.ndarray] = []
     tokens: List[np.ndarray] = []
@@ -315,7 +333,7 @@ def cfg1_tiny(seed: int = 1) -> Tuple[Batch, Batch]:
     return ext, dec
 
 
-def cfg2_decode_8b(seed: int = 2) -> Batch:
+def cfg2_decode_8b(seed: int = 2, page_size: int = 1) -> Batch:
     """Decode, Llama-3-8B attention shape: batch 64, 32 q / 8 kv heads, head_dim 128.
     Context lengths (including the new token) uniform in 512..4096; 8 groups of 8
     requests share a 1024-token system prompt (same slots); pool of 512K slots.
@@ -329,14 +347,15 @@ def cfg2_decode_8b(seed: int = 2) -> Batch:
         members = []
         for i in range(8):
             L = int(lens[g * 8 + i])
-            f = min(1024, L - 1)
+            f = min(1024, L - 1) // page_size * page_size
             specs.append(SeqSpec(L, L - 1, "decode", parent=g, fork=f))
             if f == 1024:
                 members.append(len(specs) - 1)
         if len(members) >= 2:
             groups.append((members, 1024))
-    return build_batch("cfg2_decode_8b", specs, num_slots=512 * 1024, num_q_heads=32, num_kv_heads=8,
-                       head_dim=128, seed=seed + 1, cascade=groups)
+    return build_batch("cfg2_decode_8b" if page_size == 1 else f"cfg2_decode_8b_page{page_size}", specs,
+                       num_slots=512 * 1024, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=seed + 1,
+                       cascade=groups, page_size=page_size)
 
 
 def cfg3_fewshot_extend(seed: int = 3) -> Batch:
@@ -421,7 +440,7 @@ def cfg5_multiturn_mix_70b(seed: int = 5, target_hit: float = 0.70, num_slots: i
 def random_mixed(seed: int, *, n_extend: int, n_decode: int, num_q_heads: int, num_kv_heads: int,
                  head_dim: int, max_len: int, num_slots: Optional[int] = None,
                  share_prob: float = 0.6, min_len: int = 1, with_cascade: bool = False,
-                 ext_lens: Optional[Sequence[int]] = None) -> Batch:
+                 ext_lens: Optional[Sequence[int]] = None, page_size: int = 1) -> Batch:
     """A ragged mixed batch for parity tests: random lengths in [min_len, max_len],
     random forks of earlier sequences (multi-level sharing), extend suffixes of
     random length (prefix 0 allowed), optional cascade groups of decode requests
@@ -445,6 +464,7 @@ def random_mixed(seed: int, *, n_extend: int, n_decode: int, num_q_heads: int, n
         if specs and rng.random() < share_prob:
             parent = int(rng.integers(0, len(specs)))
             fork = int(rng.integers(0, min(specs[parent].cached_len, C), endpoint=True))
+            fork = fork // page_size * page_size  # page-granular sharing
             if fork == 0:
                 parent = -1
         specs.append(SeqSpec(L, C, kinds[r], parent=parent, fork=fork))
@@ -473,10 +493,15 @@ def random_mixed(seed: int, *, n_extend: int, n_decode: int, num_q_heads: int, n
                 plen = min(plen, specs[root].total_len - 1)
             if len(members) >= 2 and plen >= 1:
                 cascade.append((members, plen))
-    total_unique = sum(s.total_len - s.fork for s in specs)
-    S = num_slots or max(64, 2 * total_unique + 8)
-    return build_batch(f"random_mixed_{seed}", specs, num_slots=S, num_q_heads=num_q_heads,
-                       num_kv_heads=num_kv_heads, head_dim=head_dim, seed=seed + 7919, cascade=cascade)
+    if page_size == 1:
+        total_unique = sum(s.total_len - s.fork for s in specs)
+        S = num_slots or max(64, 2 * total_unique + 8)
+    else:
+        pages = sum(-(-(s.total_len - s.fork) // page_size) for s in specs)
+        S = num_slots or page_size * (2 * pages + 8)
+    return build_batch(f"random_mixed_{seed}" + (f"_page{page_size}" if page_size > 1 else ""), specs,
+                       num_slots=S, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                       seed=seed + 7919, cascade=cascade, page_size=page_size)
 
 
 CONFIGS = {
