@@ -354,6 +354,24 @@ def extra_kernels(dev, flush, peaks, reps: int = 20):
     return out
 
 
+def serving_replay(dev, convs: int = 192, turns: int = 4):
+    """The radix cache driving the hot path over many steps (multi-turn chats, 70B heads, CUDA-graph
+    decode): tokens/s of the whole loop and the share of its wall time spent in the tree."""
+    from prefix_shared_kv_ra_gb300.serving import ServingReplay, multiturn_chat, run_chat
+    rp = ServingReplay(num_slots=1 << 20, num_q_heads=64, num_kv_heads=8, head_dim=128, max_len=4096,
+                       max_running=256, device=dev, seed=11)
+    chats = multiturn_chat(convs, turns, seed=11, system_prompts=8, system_len=1024, user_len=(32, 256),
+                           out_len=(16, 64))
+    st = run_chat(rp, chats, max_steps=100000, arrivals_per_step=32)
+    toks = st["extend_tokens"] + st["decode_tokens"]
+    return {"workload": f"{convs} chats x {turns} turns, 8 shared 1024-token system prompts, user 32..256, "
+                        f"output 16..64 tokens, 64 q / 8 kv heads, head_dim 128; CUDA-graph decode",
+            "steps": st["steps"], "extend_tokens": st["extend_tokens"], "decode_tokens": st["decode_tokens"],
+            "hit_ratio": round(st["hit_ratio"], 4), "tokens_per_s": toks / st["wall_s"],
+            "gpu_ms_per_step": st["gpu_ms"] / st["steps"], "wall_ms_per_step": st["wall_s"] * 1e3 / st["steps"],
+            "tree_overhead_of_wall": st["tree_overhead"], "device_error": int(rp.err.item())}
+
+
 # ----------------------------------------------------------------------------- CPU oracle arm
 def oracle_sample(b, budget_s: float, seed: int = 0):
     """Time the fp64 oracle on a random sample of the step's query rows, about `budget_s`
@@ -547,6 +565,7 @@ def main():
                 "peak_source": peaks["source"] + " HBM copy",
                 "per_launch": {"bytes": dbytes["algorithmic"], "ms": dec_ms}}
     extra = {} if args.no_extra else extra_kernels(dev, flush, peaks)
+    replay = {} if args.no_extra else serving_replay(dev)
     cpu = oracle_sample(b, args.cpu_budget)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -567,6 +586,7 @@ def main():
             "kv_store": {"gbs": store_bytes(b) / st_ms / 1e6},
             "other_workloads": extra,
         },
+        "serving_replay": replay,
         "cpu_baseline": {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
         "e2e": {"value": job_tokens / e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

@@ -95,6 +95,7 @@ class RadixCache:
         self.root = _Node(np.zeros(0, np.int32), np.zeros(0, np.int32), None)
         self.root.lock_ref = 1  # never evicted
         self._clock = 0
+        self.evictable_size = 0  # tokens in nodes no running request references (all can be evicted)
 
     # ------------------------------------------------------------------ queries
     def _tick(self) -> int:
@@ -154,6 +155,7 @@ class RadixCache:
             leaf = _Node(key[k:].copy(), val[k:].copy(), node)
             leaf.last_access = self._tick()
             node.children[int(leaf.key[0])] = leaf
+            self.evictable_size += leaf.key.size
         return k
 
     def path(self, tokens: Sequence[int]) -> List[_Node]:
@@ -168,6 +170,8 @@ class RadixCache:
     # ------------------------------------------------------------------ references
     def lock(self, node: _Node) -> None:
         while node is not None:
+            if node.lock_ref == 0:
+                self.evictable_size -= node.key.size
             node.lock_ref += 1
             node = node.parent
 
@@ -175,6 +179,8 @@ class RadixCache:
         while node is not None:
             node.lock_ref -= 1
             assert node.lock_ref >= 0
+            if node.lock_ref == 0:
+                self.evictable_size += node.key.size
             node = node.parent
 
     # ------------------------------------------------------------------ eviction
@@ -197,6 +203,7 @@ class RadixCache:
             _, _, leaf = heapq.heappop(heap)
             self.pool.free(leaf.value)
             freed += leaf.value.size
+            self.evictable_size -= leaf.key.size
             parent = leaf.parent
             del parent.children[int(leaf.key[0])]
             if parent is not self.root and not parent.children and parent.lock_ref == 0:

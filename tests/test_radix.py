@@ -145,3 +145,40 @@ def test_paged_eviction_frees_whole_pages():
     assert pool.available() == free0 + 16
     assert cache.evict(100) == 32                    # the other leaf, then the shared parent
     assert pool.available() == 120
+
+
+def test_evictable_size_tracks_locks_inserts_and_evictions():
+    rng = np.random.default_rng(5)
+    pool = SlotPool(4096)
+    cache = RadixCache(pool)
+    locked = []
+
+    def brute():
+        out, stack = 0, [cache.root]
+        while stack:
+            n = stack.pop()
+            if n is not cache.root and n.lock_ref == 0:
+                out += n.key.size
+            stack.extend(n.children.values())
+        return out
+
+    for step in range(300):
+        op = rng.integers(0, 4)
+        if op <= 1:  # a request: match, lock, insert its sequence
+            base = [int(x) for x in rng.integers(0, 4, size=int(rng.integers(1, 4)))]
+            seq = base + [int(x) for x in rng.integers(0, 50, size=int(rng.integers(1, 20)))]
+            hit, node = cache.match_prefix(seq)
+            cache.lock(node)
+            locked.append(node)
+            slots = pool.alloc(len(seq) - hit.size)
+            if slots is None:
+                cache.unlock(locked.pop())
+                continue
+            kept = cache.insert(seq, np.concatenate([hit, slots]))
+            if kept > hit.size:
+                pool.free(slots[:kept - hit.size])
+        elif op == 2 and locked:
+            cache.unlock(locked.pop(int(rng.integers(0, len(locked)))))
+        else:
+            cache.evict(int(rng.integers(1, 40)))
+        assert cache.evictable_size == brute(), step
