@@ -165,11 +165,17 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def with_tree_groups(b, min_prefix: int = 256):
-    """Attach the cascade groups the radix tree derives from the batch's decode table rows."""
-    from prefix_shared_kv_ra_gb300.radix import cascade_groups
+def with_tree_groups(b, min_prefix: int = 256, multilevel: bool = False):
+    """Attach the cascade groups the radix tree derives from the batch's decode table rows: one level
+    (per subtree of the root, prefixes of >= min_prefix tokens) or one group per shared node."""
+    from prefix_shared_kv_ra_gb300.radix import cascade_groups, cascade_groups_multilevel
     rows = [b.req_to_token[r, :L] for r, L in zip(b.dec_rpi, b.dec_seq_lens)]
-    b.casc_group_indptr, b.casc_group_reqs, b.casc_group_prefix_len = cascade_groups(rows, min_prefix=min_prefix)
+    if multilevel:
+        (b.casc_group_indptr, b.casc_group_reqs, b.casc_group_start, b.casc_group_prefix_len, b.casc_group_level,
+         b.casc_levels) = cascade_groups_multilevel(rows, min_range=min_prefix)
+    else:
+        b.casc_group_indptr, b.casc_group_reqs, b.casc_group_prefix_len = cascade_groups(rows, min_prefix=min_prefix)
+        b.casc_group_start, b.casc_group_level, b.casc_levels = None, None, 1
     return b
 
 
@@ -209,11 +215,14 @@ class Step:
             self.casc = dict(group_indptr=i32(b.casc_group_indptr), group_reqs=i32(b.casc_group_reqs),
                              group_prefix_len=i32(b.casc_group_prefix_len),
                              max_group_prefix_len=int(b.casc_group_prefix_len.max()),
-                             max_group_size=int(np.diff(b.casc_group_indptr).max()))
+                             max_group_size=int(np.diff(b.casc_group_indptr).max()),
+                             group_prefix_start=None if b.casc_group_start is None else i32(b.casc_group_start),
+                             group_level=None if b.casc_group_level is None else i32(b.casc_group_level),
+                             max_group_levels=int(b.casc_levels))
         ng = b.casc_group_indptr.size - 1 if self.cascade else 0
         nws = ra.ra_decode_workspace_bytes(max(b.n_decode, 1), b.num_q_heads, hkv, d, max(b.max_seq_len, 1), ng,
                                            self.casc.get("max_group_prefix_len", 0),
-                                           self.casc.get("max_group_size", 0))
+                                           self.casc.get("max_group_size", 0), self.casc.get("max_group_levels", 1))
         self.ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
         self.ext_ws = torch.empty(max(ra.ra_extend_workspace_bytes(b.n_extend, b.total_q_extend, b.num_q_heads, hkv),
                                       256), dtype=torch.uint8, device=dev)

@@ -147,33 +147,44 @@ size_t ra_extend_workspace_bytes(int32_t batch, int64_t total_q, int32_t num_q_h
  * combine pass; the partial results live in `workspace`.
  *
  * Optional prefix-grouped (cascade) read, num_groups > 0: group g lists
- * decode requests group_reqs[group_indptr[g] .. group_indptr[g+1]) whose first
- * group_prefix_len[g] table entries are the same slots (a shared radix-tree
- * prefix).  That prefix is read from HBM once per group and kv head for all
- * members (the yaopepe.com explainer, §04 figure: the shared prefix's KV is
- * stored once and referenced by every branch); each member then reads only
- * its own positions group_prefix_len[g]..seq_lens[b]-1, and the two partial
+ * decode requests group_reqs[group_indptr[g] .. group_indptr[g+1]) whose table
+ * entries at positions group_prefix_start[g] .. group_prefix_len[g]-1 are the
+ * same slots (a node of the radix tree they all pass through).  Those keys are
+ * read from HBM once per group and kv head for all members (the yaopepe.com
+ * explainer, §04 figure: the shared prefix's KV is stored once and referenced
+ * by every branch); each member then reads only its own positions from the
+ * largest group_prefix_len of its groups to seq_lens[b]-1, and all partial
  * results are merged exactly.  The result equals the non-grouped call up to
- * floating-point rounding.  Preconditions: every request is in at most one
- * group, 1 <= group_prefix_len[g] <= seq_lens[b] for each member, the members'
- * table rows agree on the prefix (the prefix is read through the first
- * member's row).  max_group_prefix_len / max_group_size are host-side bounds.
- * With num_groups == 0 the group pointers may be NULL.
+ * floating-point rounding.
+ *   Multi-level: a request may be in up to max_group_levels groups, one per
+ *   level, group_level[g] in [0, max_group_levels); its groups' ranges must be
+ *   disjoint and together cover positions 0 .. (largest group_prefix_len)-1
+ *   (the nested nodes of one path from the root of the tree).
+ *   group_prefix_start may be NULL (all 0) and group_level NULL (all 0: one
+ *   group per request at most).
+ *   Preconditions: 0 <= group_prefix_start[g] < group_prefix_len[g] <=
+ *   seq_lens[b] for each member; the members' table rows agree on the range
+ *   (it is read through the first member's row).  max_group_prefix_len (bound
+ *   of group_prefix_len), max_group_size and max_group_levels are host-side
+ *   bounds; a device value outside them is flagged and its group skipped.
+ *   With num_groups == 0 the group pointers may be NULL.
  */
 ra_status ra_decode_attention(const void* k_pool, const void* v_pool, int64_t num_slots, int32_t num_kv_heads,
                               int32_t head_dim, const void* q, void* o, int32_t num_q_heads, float sm_scale,
                               const int32_t* req_to_token, int64_t table_stride, int64_t table_rows,
                               const int32_t* req_pool_indices, const int32_t* seq_lens, int32_t batch,
                               int32_t max_seq_len, int32_t num_groups, const int32_t* group_indptr,
-                              const int32_t* group_reqs, const int32_t* group_prefix_len,
-                              int32_t max_group_prefix_len, int32_t max_group_size, void* workspace,
+                              const int32_t* group_reqs, const int32_t* group_prefix_start,
+                              const int32_t* group_prefix_len, const int32_t* group_level,
+                              int32_t max_group_prefix_len, int32_t max_group_size, int32_t max_group_levels,
+                              void* workspace,
                               size_t workspace_bytes, uint32_t* device_error, ra_stream_t stream);
 
 /* Bytes of workspace ra_decode_attention needs for these host-side bounds
  * (same arguments as the call).  Depends on nothing else. */
 size_t ra_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                  int32_t max_seq_len, int32_t num_groups, int32_t max_group_prefix_len,
-                                 int32_t max_group_size);
+                                 int32_t max_group_size, int32_t max_group_levels);
 
 /*
  * ra_decode_attention_static -- ra_decode_attention for callers that cannot
@@ -199,8 +210,10 @@ ra_status ra_decode_attention_static(const void* k_pool, const void* v_pool, int
                                      int64_t table_stride, int64_t table_rows, const int32_t* req_pool_indices,
                                      const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
                                      int32_t num_groups, const int32_t* group_indptr, const int32_t* group_reqs,
-                                     const int32_t* group_prefix_len, int32_t max_group_prefix_len,
-                                     int32_t max_group_size, uint32_t* device_error, ra_stream_t stream);
+                                     const int32_t* group_prefix_start, const int32_t* group_prefix_len,
+                                     const int32_t* group_level, int32_t max_group_prefix_len,
+                                     int32_t max_group_size, int32_t max_group_levels, uint32_t* device_error,
+                                     ra_stream_t stream);
 
 /* Static description of a status code. */
 const char* ra_status_string(ra_status status);
@@ -211,7 +224,7 @@ const char* ra_last_error_message(void);
 /* ABI revision of this header (bumped on any signature change). */
 int32_t ra_abi_version(void);
 
-#define RA_ABI_VERSION 2
+#define RA_ABI_VERSION 3
 
 #ifdef __cplusplus
 }

@@ -61,11 +61,11 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.ra_extend_workspace_bytes.argtypes = [i32, i64, i32, i32]
     lib.ra_extend_workspace_bytes.restype = sz
     lib.ra_decode_attention.argtypes = [P, P, i64, i32, i32, P, P, i32, f32, P, i64, i64, P, P, i32, i32, i32,
-                                        P, P, P, i32, i32, P, sz, P, P]
+                                        P, P, P, P, P, i32, i32, i32, P, sz, P, P]
     lib.ra_decode_attention_static.argtypes = [P, P, i64, i32, i32, P, P, i32, f32, P, i64, i64, P, P, i32, i32,
-                                               i32, P, P, P, i32, i32, P, P]
+                                               i32, P, P, P, P, P, i32, i32, i32, P, P]
     lib.ra_decode_attention_static.restype = ctypes.c_int
-    lib.ra_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+    lib.ra_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32]
     lib.ra_decode_workspace_bytes.restype = sz
     for f in (lib.ra_kv_store, lib.ra_extend_attention, lib.ra_decode_attention, lib.ra_abi_version):
         f.restype = ctypes.c_int
@@ -151,9 +151,10 @@ def ra_extend_workspace_bytes(batch: int, total_q: int, num_q_heads: int, num_kv
 
 
 def ra_decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, max_seq_len: int,
-                              num_groups: int = 0, max_group_prefix_len: int = 0, max_group_size: int = 0) -> int:
+                              num_groups: int = 0, max_group_prefix_len: int = 0, max_group_size: int = 0,
+                              max_group_levels: int = 1) -> int:
     return int(load().ra_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
-                                                num_groups, max_group_prefix_len, max_group_size))
+                                                num_groups, max_group_prefix_len, max_group_size, max_group_levels))
 
 
 def ra_decode_attention(k_pool: torch.Tensor, v_pool: torch.Tensor, q: torch.Tensor, o: torch.Tensor,
@@ -161,9 +162,11 @@ def ra_decode_attention(k_pool: torch.Tensor, v_pool: torch.Tensor, q: torch.Ten
                         max_seq_len: int, sm_scale: float, workspace: torch.Tensor,
                         group_indptr: Optional[torch.Tensor] = None, group_reqs: Optional[torch.Tensor] = None,
                         group_prefix_len: Optional[torch.Tensor] = None, max_group_prefix_len: int = 0,
-                        max_group_size: int = 0, device_error: Optional[torch.Tensor] = None,
-                        stream=None) -> None:
-    """One query per request over its context; q, o [batch, Hq, D] bf16; optional cascade groups."""
+                        max_group_size: int = 0, group_prefix_start: Optional[torch.Tensor] = None,
+                        group_level: Optional[torch.Tensor] = None, max_group_levels: int = 1,
+                        device_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """One query per request over its context; q, o [batch, Hq, D] bf16; optional cascade groups (group g
+    covers positions group_prefix_start[g] .. group_prefix_len[g]-1 of its members, at group_level[g])."""
     dev = k_pool.device
     S, hkv, d = k_pool.shape
     batch, hq, dq = q.shape
@@ -179,9 +182,10 @@ def ra_decode_attention(k_pool: torch.Tensor, v_pool: torch.Tensor, q: torch.Ten
         req_to_token.shape[1], req_to_token.shape[0], _ptr(req_pool_indices, i32, "req_pool_indices", dev),
         _ptr(seq_lens, i32, "seq_lens", dev), batch, int(max_seq_len), ng,
         _ptr(group_indptr, i32, "group_indptr", dev), _ptr(group_reqs, i32, "group_reqs", dev),
-        _ptr(group_prefix_len, i32, "group_prefix_len", dev), int(max_group_prefix_len), int(max_group_size),
-        ctypes.c_void_p(workspace.data_ptr()), workspace.numel(), _ptr(device_error, i32, "device_error", dev),
-        _stream(dev, stream)))
+        _ptr(group_prefix_start, i32, "group_prefix_start", dev), _ptr(group_prefix_len, i32, "group_prefix_len", dev),
+        _ptr(group_level, i32, "group_level", dev), int(max_group_prefix_len), int(max_group_size),
+        int(max_group_levels), ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+        _ptr(device_error, i32, "device_error", dev), _stream(dev, stream)))
 
 
 def ra_decode_attention_static(k_pool: torch.Tensor, v_pool: torch.Tensor, q: torch.Tensor, o: torch.Tensor,
@@ -189,8 +193,9 @@ def ra_decode_attention_static(k_pool: torch.Tensor, v_pool: torch.Tensor, q: to
                                max_seq_len: int, sm_scale: float, group_indptr: Optional[torch.Tensor] = None,
                                group_reqs: Optional[torch.Tensor] = None,
                                group_prefix_len: Optional[torch.Tensor] = None, max_group_prefix_len: int = 0,
-                               max_group_size: int = 0, device_error: Optional[torch.Tensor] = None,
-                               stream=None) -> None:
+                               max_group_size: int = 0, group_prefix_start: Optional[torch.Tensor] = None,
+                               group_level: Optional[torch.Tensor] = None, max_group_levels: int = 1,
+                               device_error: Optional[torch.Tensor] = None, stream=None) -> None:
     """ra_decode_attention without a workspace argument, for callers that cannot allocate:
     the library's static device scratch (RA_DECODE_STATIC_SCRATCH_BYTES) is used instead."""
     dev = k_pool.device
@@ -206,5 +211,6 @@ def ra_decode_attention_static(k_pool: torch.Tensor, v_pool: torch.Tensor, q: to
         req_to_token.shape[1], req_to_token.shape[0], _ptr(req_pool_indices, i32, "req_pool_indices", dev),
         _ptr(seq_lens, i32, "seq_lens", dev), batch, int(max_seq_len), ng,
         _ptr(group_indptr, i32, "group_indptr", dev), _ptr(group_reqs, i32, "group_reqs", dev),
-        _ptr(group_prefix_len, i32, "group_prefix_len", dev), int(max_group_prefix_len), int(max_group_size),
-        _ptr(device_error, i32, "device_error", dev), _stream(dev, stream)))
+        _ptr(group_prefix_start, i32, "group_prefix_start", dev), _ptr(group_prefix_len, i32, "group_prefix_len", dev),
+        _ptr(group_level, i32, "group_level", dev), int(max_group_prefix_len), int(max_group_size),
+        int(max_group_levels), _ptr(device_error, i32, "device_error", dev), _stream(dev, stream)))

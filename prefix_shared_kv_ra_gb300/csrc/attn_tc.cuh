@@ -74,7 +74,11 @@ struct TcParams {
   // cascade prefix pass
   const int32_t* group_indptr;
   const int32_t* group_reqs;
-  const int32_t* group_prefix_len;
+  const int32_t* group_prefix_start;  // nullable: 0
+  const int32_t* group_prefix_len;    // end of the group's range
+  const int32_t* group_level;         // nullable: 0
+  int32_t casc_levels;                // levels of prefix partials per member
+  int32_t casc_slots;                 // casc_levels x max_csplits
   int32_t num_groups;
   int32_t grid_x;  // member tiles x prefix splits per group
   int32_t batch;   // decode batch (bound for group_reqs entries)
@@ -132,6 +136,7 @@ struct Job {
   int64_t q_tok0;    // extend: first q token
   int32_t mem0;      // cascade: first member index into group_reqs
   int32_t csplit;    // cascade: prefix split
+  int32_t slot;      // cascade: partial slot of the members (level x max_csplits + split)
 };
 
 // Item -> job; false for an empty or invalid item (reported once, when `report`).
@@ -144,6 +149,7 @@ __device__ __forceinline__ bool tc_job(const TcParams& p, int32_t item, Job& j, 
   j.q_tok0 = 0;
   j.mem0 = 0;
   j.csplit = 0;
+  j.slot = 0;
   if constexpr (EXTEND) {
     // entry `rest` of the work list: it holds only non-empty query tiles of requests whose lengths
     // were checked (and flagged) when it was built
@@ -169,14 +175,18 @@ __device__ __forceinline__ bool tc_job(const TcParams& p, int32_t item, Job& j, 
     const int mt = x / p.max_csplits;
     j.csplit = x - mt * p.max_csplits;
     if (mt * kTiles * T >= n_mem) return false;
+    // the group's range [g0, Pg) of its members' positions, split into cchunk-key pieces
     const int32_t Pg = __ldg(p.group_prefix_len + g);
-    if (Pg < 1 || Pg > p.max_seq_len) {
+    const int32_t g0 = p.group_prefix_start ? __ldg(p.group_prefix_start + g) : 0;
+    const int32_t lvl = p.group_level ? __ldg(p.group_level + g) : 0;
+    if (Pg < 1 || Pg > p.max_seq_len || g0 < 0 || g0 >= Pg || lvl < 0 || lvl >= p.casc_levels) {
       if (report && x == 0 && j.kh == 0) flag_error(p.err, RA_DEVERR_LENGTH);
       return false;
     }
-    if (j.csplit * p.cchunk >= Pg) return false;
-    j.kbeg = j.csplit * p.cchunk;
+    if (j.csplit * p.cchunk >= Pg - g0) return false;
+    j.kbeg = g0 + j.csplit * p.cchunk;
     j.kend = min(Pg, j.kbeg + p.cchunk);
+    j.slot = lvl * p.max_csplits + j.csplit;
     j.mem0 = m_begin + mt * kTiles * T;
     j.n_valid = min(kTiles * T, n_mem - mt * kTiles * T);
     const int32_t leader = __ldg(p.group_reqs + m_begin);
@@ -724,7 +734,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         int32_t b = __ldg(p.group_reqs + jb.mem0 + (row_valid ? tok : 0));
         const bool write = row_valid && b >= 0 && b < p.batch;
         const int64_t ps =
-            ((static_cast<int64_t>(write ? b : 0) * p.hq + jb.kh * G + (r % G)) * p.max_csplits + jb.csplit);
+            ((static_cast<int64_t>(write ? b : 0) * p.hq + jb.kh * G + (r % G)) * p.casc_slots + jb.slot);
         float* dst = p.casc_o + ps * D;
         uint32_t oa[D / 32][32];
 #pragma unroll

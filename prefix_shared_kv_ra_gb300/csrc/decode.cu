@@ -393,12 +393,13 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
   int32_t start = p.key_start ? __ldg(p.key_start + b) : 0;
   start = start < 0 ? 0 : (start > L ? L : start);
   const int32_t n_splits = (L - start + p.chunk - 1) / p.chunk;
-  const int32_t n_pre = start > 0 ? (start + p.cchunk - 1) / p.cchunk : 0;
+  // prefix partials: every slot of every level; those no group wrote hold -inf (weight 0, skipped)
+  const int32_t n_pre = start > 0 ? p.casc_slots : 0;
   if (n_splits == 1 && n_pre == 0) return;  // written directly by the decode kernel
   const int32_t n = n_pre + n_splits;
   const int64_t bh = warp_global;
   auto lse_of = [&](int s) {
-    return s < n_pre ? p.casc_lse[bh * p.max_csplits + s] : p.part_lse[bh * p.max_splits + (s - n_pre)];
+    return s < n_pre ? p.casc_lse[bh * p.casc_slots + s] : p.part_lse[bh * p.max_splits + (s - n_pre)];
   };
   float mm = -INFINITY;
   for (int base = 0; base < n; base += 32)
@@ -417,7 +418,8 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
     for (int k = 0; k < cnt; ++k) {
       const int s = base + k;
       const float w = __shfl_sync(0xffffffffu, wl, k);
-      const float* src = s < n_pre ? p.casc_o + (bh * p.max_csplits + s) * D
+      if (w == 0.f) continue;  // an empty prefix slot (its partial was never written)
+      const float* src = s < n_pre ? p.casc_o + (bh * p.casc_slots + s) * D
                                    : p.part_o + (bh * p.max_splits + (s - n_pre)) * D;
 #pragma unroll
       for (int v = 0; v < V; ++v) acc[v] += w * src[lane * V + v];
@@ -432,12 +434,16 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
         __floats2bfloat162_rn(acc[v] * inv, acc[v + 1] * inv);
 }
 
-// key_start[b] = prefix length of b's cascade group (0 for requests in no group, set by the memset).
+// key_start[b] = the largest range end of b's cascade groups (0 for requests in no group, set by the
+// memset); every prefix-partial slot's log-sum-exp starts at -inf (slots no group writes stay so).
 __global__ void cascade_key_start_kernel(int32_t* key_start, int32_t batch, const int32_t* group_indptr,
                                          const int32_t* group_reqs, const int32_t* group_prefix_len,
-                                         int32_t num_groups, uint32_t* err) {
+                                         int32_t num_groups, float* casc_lse, int64_t n_lse, uint32_t* err) {
   griddep_wait();
   griddep_launch();
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n_lse;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    casc_lse[i] = -INFINITY;
   const int32_t total = __ldg(group_indptr + num_groups);
   for (int32_t m = blockIdx.x * blockDim.x + threadIdx.x; m < total; m += gridDim.x * blockDim.x) {
     int32_t lo = 0, hi = num_groups;  // group g with indptr[g] <= m < indptr[g+1]
@@ -450,7 +456,7 @@ __global__ void cascade_key_start_kernel(int32_t* key_start, int32_t batch, cons
       flag_error(err, RA_DEVERR_TABLE);
       continue;
     }
-    key_start[b] = __ldg(group_prefix_len + lo);
+    atomicMax(key_start + b, __ldg(group_prefix_len + lo));
   }
 }
 
@@ -529,7 +535,7 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
 }
 
 DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
-                                        int32_t head_dim, const DecodePlan& pl, bool cascade) {
+                                        int32_t head_dim, const DecodePlan& pl, int32_t cascade_levels) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   DecodeWorkspace w;
   const size_t bh = static_cast<size_t>(batch) * num_q_heads;
@@ -538,11 +544,12 @@ DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int3
   off += up(bh * pl.max_splits * head_dim * sizeof(float));
   w.part_lse = off;
   off += up(bh * pl.max_splits * sizeof(float));
-  if (cascade) {
+  if (cascade_levels > 0) {
+    const size_t slots = static_cast<size_t>(cascade_levels) * pl.max_csplits;
     w.casc_o = off;
-    off += up(bh * pl.max_csplits * head_dim * sizeof(float));
+    off += up(bh * slots * head_dim * sizeof(float));
     w.casc_lse = off;
-    off += up(bh * pl.max_csplits * sizeof(float));
+    off += up(bh * slots * sizeof(float));
   }
   w.ints = off;
   (void)num_kv_heads;
@@ -556,12 +563,15 @@ DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int3
 
 extern "C" size_t ra_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                             int32_t head_dim, int32_t max_seq_len, int32_t num_groups,
-                                            int32_t max_group_prefix_len, int32_t max_group_size) {
+                                            int32_t max_group_prefix_len, int32_t max_group_size,
+                                            int32_t max_group_levels) {
   if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
-  if (num_groups > 0 && (max_group_prefix_len <= 0 || max_group_size <= 0)) return 0;
+  if (num_groups > 0 && (max_group_prefix_len <= 0 || max_group_size <= 0 || max_group_levels <= 0)) return 0;
   const ra::DecodePlan pl = ra::plan_decode(batch, num_q_heads, num_kv_heads, max_seq_len, num_groups,
                                             max_group_prefix_len, max_group_size);
-  return ra::layout_decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, pl, num_groups > 0).total;
+  return ra::layout_decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, pl,
+                                     num_groups > 0 ? max_group_levels : 0)
+      .total;
 }
 
 extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool, int64_t num_slots,
@@ -570,9 +580,11 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
                                          int64_t table_stride, int64_t table_rows, const int32_t* req_pool_indices,
                                          const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
                                          int32_t num_groups, const int32_t* group_indptr,
-                                         const int32_t* group_reqs, const int32_t* group_prefix_len,
-                                         int32_t max_group_prefix_len, int32_t max_group_size, void* workspace,
-                                         size_t workspace_bytes, uint32_t* device_error, ra_stream_t stream) {
+                                         const int32_t* group_reqs, const int32_t* group_prefix_start,
+                                         const int32_t* group_prefix_len, const int32_t* group_level,
+                                         int32_t max_group_prefix_len, int32_t max_group_size,
+                                         int32_t max_group_levels, void* workspace, size_t workspace_bytes,
+                                         uint32_t* device_error, ra_stream_t stream) {
   using namespace ra;
   clear_error();
   RA_REQUIRE(batch >= 0 && batch <= 65535, "batch must be in [0, 65535] (got %d)", batch);
@@ -600,10 +612,16 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
     RA_REQUIRE(max_group_prefix_len >= 1 && max_group_prefix_len <= max_seq_len,
                "max_group_prefix_len must be in [1, max_seq_len]");
     RA_REQUIRE(max_group_size >= 1 && max_group_size <= batch, "max_group_size must be in [1, batch]");
+    RA_REQUIRE(max_group_levels >= 1 && max_group_levels <= 64, "max_group_levels must be in [1, 64]");
+    RA_REQUIRE(group_level || max_group_levels == 1, "max_group_levels > 1 needs group_level");
+    RA_REQUIRE(aligned4(group_indptr) && aligned4(group_reqs) && aligned4(group_prefix_len) &&
+                   (!group_prefix_start || aligned4(group_prefix_start)) && (!group_level || aligned4(group_level)),
+               "group arrays must be 4-byte aligned");
   }
   const DecodePlan pl = plan_decode(batch, num_q_heads, num_kv_heads, max_seq_len, num_groups,
                                     max_group_prefix_len, max_group_size);
-  const DecodeWorkspace wl = layout_decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, pl, num_groups > 0);
+  const int32_t levels = num_groups > 0 ? max_group_levels : 0;
+  const DecodeWorkspace wl = layout_decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, pl, levels);
   if (workspace_bytes < wl.total)
     return fail(RA_ERR_WORKSPACE, "workspace of %zu bytes, need %zu", workspace_bytes, wl.total);
   RA_REQUIRE(workspace && aligned16(workspace), "workspace must be non-null and 16-byte aligned");
@@ -641,14 +659,16 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
   if (num_groups > 0) {
     p.cchunk = pl.cchunk;
     p.max_csplits = pl.max_csplits;
+    p.casc_slots = levels * pl.max_csplits;
     p.casc_o = reinterpret_cast<float*>(ws + wl.casc_o);
     p.casc_lse = reinterpret_cast<float*>(ws + wl.casc_lse);
     p.key_start = ints;
     if (ra_status st = launch_pdl("cascade_key_start_kernel", cascade_key_start_kernel, dim3((batch + 127) / 128),
                                   dim3(128), 0, s, ints, batch, group_indptr, group_reqs, group_prefix_len, num_groups,
-                                  device_error))
+                                  p.casc_lse, static_cast<int64_t>(batch) * num_q_heads * p.casc_slots, device_error))
       return st;
-    CascadeArgs ca{group_indptr, group_reqs, group_prefix_len, num_groups, max_group_prefix_len, max_group_size};
+    CascadeArgs ca{group_indptr,         group_reqs,           group_prefix_start, group_prefix_len, group_level,
+                   num_groups,           max_group_prefix_len, max_group_size,     max_group_levels};
     if (ra_status st = launch_cascade_prefix(p, ca, head_dim, s)) return st;
   }
   // persistent decode geometry

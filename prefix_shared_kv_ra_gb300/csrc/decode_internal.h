@@ -44,9 +44,10 @@ struct DecodeParams {
   float* part_o;    // [batch, hq, max_splits, D]
   float* part_lse;  // [batch, hq, max_splits] (log2 domain)
   int32_t cchunk;      // shared-prefix keys per prefix-pass split (cascade)
-  int32_t max_csplits;  // prefix-pass splits per member
-  float* casc_o;        // [batch, hq, max_csplits, D] shared-prefix partials (cascade)
-  float* casc_lse;      // [batch, hq, max_csplits]
+  int32_t max_csplits;  // prefix-pass splits per group range
+  int32_t casc_slots;   // prefix partials per (request, q head): levels x max_csplits
+  float* casc_o;        // [batch, hq, casc_slots, D] shared-prefix partials (cascade)
+  float* casc_lse;      // [batch, hq, casc_slots]; -inf marks a slot no group wrote
   uint32_t* err;
 };
 
@@ -68,16 +69,19 @@ constexpr int kMaxHeadsPerCta = 8;  // consumer warps of the decode kernel
 struct CascadeArgs {
   const int32_t* group_indptr;
   const int32_t* group_reqs;
-  const int32_t* group_prefix_len;
+  const int32_t* group_prefix_start;  // nullable: 0
+  const int32_t* group_prefix_len;    // end position of the group's range
+  const int32_t* group_level;         // nullable: 0
   int32_t num_groups;
   int32_t max_group_prefix_len;
   int32_t max_group_size;
+  int32_t max_group_levels;
 };
 
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seq_len,
                        int32_t num_groups, int32_t max_group_prefix_len, int32_t max_group_size);
 DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
-                                        int32_t head_dim, const DecodePlan& pl, bool cascade);
+                                        int32_t head_dim, const DecodePlan& pl, int32_t cascade_levels);
 
 // Tensor-core pass over each group's shared prefix: writes p.casc_o / p.casc_lse
 // for every member (defined with the tcgen05 attention kernel).

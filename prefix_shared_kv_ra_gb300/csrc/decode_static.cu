@@ -59,14 +59,15 @@ extern "C" ra_status ra_decode_attention_static(
     const void* k_pool, const void* v_pool, int64_t num_slots, int32_t num_kv_heads, int32_t head_dim, const void* q,
     void* o, int32_t num_q_heads, float sm_scale, const int32_t* req_to_token, int64_t table_stride,
     int64_t table_rows, const int32_t* req_pool_indices, const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
-    int32_t num_groups, const int32_t* group_indptr, const int32_t* group_reqs, const int32_t* group_prefix_len,
-    int32_t max_group_prefix_len, int32_t max_group_size, uint32_t* device_error, ra_stream_t stream) {
+    int32_t num_groups, const int32_t* group_indptr, const int32_t* group_reqs, const int32_t* group_prefix_start,
+    const int32_t* group_prefix_len, const int32_t* group_level, int32_t max_group_prefix_len, int32_t max_group_size,
+    int32_t max_group_levels, uint32_t* device_error, ra_stream_t stream) {
   using namespace ra;
   clear_error();
   void* scratch = nullptr;
   if (ra_status st = scratch_for_current_device(&scratch)) return st;
   const size_t need = ra_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len,
-                                                num_groups, max_group_prefix_len, max_group_size);
+                                                num_groups, max_group_prefix_len, max_group_size, max_group_levels);
   if (need > static_cast<size_t>(RA_DECODE_STATIC_SCRATCH_BYTES))
     return fail(RA_ERR_WORKSPACE,
                 "this decode needs %zu bytes of scratch; the static scratch holds %zu "
@@ -74,7 +75,7 @@ extern "C" ra_status ra_decode_attention_static(
                 need, static_cast<size_t>(RA_DECODE_STATIC_SCRATCH_BYTES));
   return ra_decode_attention(k_pool, v_pool, num_slots, num_kv_heads, head_dim, q, o, num_q_heads, sm_scale,
                              req_to_token, table_stride, table_rows, req_pool_indices, seq_lens, batch, max_seq_len,
-                             num_groups, group_indptr, group_reqs, group_prefix_len, max_group_prefix_len,
-                             max_group_size, scratch, static_cast<size_t>(RA_DECODE_STATIC_SCRATCH_BYTES),
-                             device_error, stream);
+                             num_groups, group_indptr, group_reqs, group_prefix_start, group_prefix_len, group_level,
+                             max_group_prefix_len, max_group_size, max_group_levels, scratch,
+                             static_cast<size_t>(RA_DECODE_STATIC_SCRATCH_BYTES), device_error, stream);
 }

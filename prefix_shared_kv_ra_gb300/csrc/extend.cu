@@ -260,7 +260,11 @@ ra_status launch_cascade_prefix(const DecodeParams& d, const CascadeArgs& ca, in
   p.rpi = d.rpi;
   p.group_indptr = ca.group_indptr;
   p.group_reqs = ca.group_reqs;
+  p.group_prefix_start = ca.group_prefix_start;
   p.group_prefix_len = ca.group_prefix_len;
+  p.group_level = ca.group_level;
+  p.casc_levels = ca.max_group_levels;
+  p.casc_slots = d.casc_slots;
   p.batch = d.batch;
   p.max_seq_len = d.max_seq_len;
   p.cchunk = d.cchunk;

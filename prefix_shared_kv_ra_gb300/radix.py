@@ -261,3 +261,55 @@ def cascade_groups(paths: Sequence[Sequence[int]], min_prefix: int = 1,
         indptr.append(len(reqs))
         plens.append(plen)
     return (np.asarray(indptr, np.int32), np.asarray(reqs, np.int32), np.asarray(plens, np.int32))
+
+
+def cascade_groups_multilevel(paths: Sequence[Sequence[int]], min_members: int = 2, min_range: int = 1):
+    """Multi-level cascade groups for a decode batch: groups over the nodes of the tree of the requests'
+    slot rows (each cut one token short, so every request keeps its newest token private) that at
+    least `min_members` requests pass through.  A group covers positions [start, end) of its members,
+    where end is its node's end and start the end of the group above it (0 at the top); a node whose
+    range so far is shorter than `min_range` forms no group, and its positions go to the groups below
+    it (its members that end there read them privately).  A group's level is the number of groups
+    above it, so each request's groups cover positions 0 .. (its deepest end) - 1 without gaps.
+
+    Returns (group_indptr, group_reqs, group_start, group_end, group_level, max_levels)."""
+    root = {"key": np.zeros(0, np.int64), "children": {}, "reqs": []}
+    for b, row in enumerate(paths):
+        seq = np.asarray(row, dtype=np.int64)[:max(len(row) - 1, 0)]
+        node, pos = root, 0
+        while pos < seq.size:
+            child = node["children"].get(int(seq[pos]))
+            if child is None:
+                leaf = {"key": seq[pos:].copy(), "children": {}, "reqs": [b]}
+                node["children"][int(seq[pos])] = leaf
+                pos = seq.size
+                break
+            k = _common_len(child["key"], seq[pos:])
+            if k < child["key"].size:  # split the edge at k
+                mid = {"key": child["key"][:k].copy(), "children": {}, "reqs": list(child["reqs"])}
+                child["key"] = child["key"][k:].copy()
+                mid["children"][int(child["key"][0])] = child
+                node["children"][int(mid["key"][0])] = mid
+                child = mid
+            child["reqs"].append(b)
+            node = child
+            pos += k
+    indptr, reqs, starts, ends, levels = [0], [], [], [], []
+    max_levels = 0
+    stack = [(root, 0, 0, 0)]  # node, depth at its start, start of its pending range, groups above it
+    while stack:
+        node, depth, pending, lvl = stack.pop()
+        end = depth + node["key"].size
+        is_group = node is not root and len(node["reqs"]) >= min_members and end - pending >= min_range
+        if is_group:
+            reqs.extend(sorted(node["reqs"]))
+            indptr.append(len(reqs))
+            starts.append(pending)
+            ends.append(end)
+            levels.append(lvl)
+            max_levels = max(max_levels, lvl + 1)
+        for c in node["children"].values():
+            if len(c["reqs"]) >= min_members:  # only shared nodes can hold groups
+                stack.append((c, end, end if is_group else pending, lvl + (1 if is_group else 0)))
+    a = lambda x: np.asarray(x, np.int32)
+    return a(indptr), a(reqs), a(starts), a(ends), a(levels), max_levels

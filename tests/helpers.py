@@ -54,6 +54,8 @@ class DeviceBatch:
             self.g_indptr = i32(b.casc_group_indptr, self.dev)
             self.g_reqs = i32(b.casc_group_reqs, self.dev)
             self.g_plen = i32(b.casc_group_prefix_len, self.dev)
+            self.g_start = None if b.casc_group_start is None else i32(b.casc_group_start, self.dev)
+            self.g_level = None if b.casc_group_level is None else i32(b.casc_group_level, self.dev)
         self.ext_o = torch.empty_like(self.ext_q)
         self.dec_o = torch.empty_like(self.dec_q)
         self.ws = torch.empty(0, dtype=torch.uint8, device=self.dev)
@@ -81,7 +83,7 @@ class DeviceBatch:
             mp = int(b.casc_group_prefix_len.max())
             ms = int(np.diff(b.casc_group_indptr).max())
         n = ra.ra_decode_workspace_bytes(b.n_decode, b.num_q_heads, b.num_kv_heads, b.head_dim, b.max_seq_len,
-                                         ng, mp, ms)
+                                         ng, mp, ms, b.casc_levels if cascade else 1)
         if self.ws.numel() < n:
             self.ws = torch.empty(n, dtype=torch.uint8, device=self.dev)
         return self.ws
@@ -95,7 +97,8 @@ class DeviceBatch:
         if cascade:
             kw = dict(group_indptr=self.g_indptr, group_reqs=self.g_reqs, group_prefix_len=self.g_plen,
                       max_group_prefix_len=int(b.casc_group_prefix_len.max()),
-                      max_group_size=int(np.diff(b.casc_group_indptr).max()))
+                      max_group_size=int(np.diff(b.casc_group_indptr).max()), group_prefix_start=self.g_start,
+                      group_level=self.g_level, max_group_levels=b.casc_levels)
         ra.ra_decode_attention(self.k_pool, self.v_pool, self.dec_q, self.dec_o, self.table, self.dec_rpi,
                                self.dec_lens, max_seq_len=b.max_seq_len, sm_scale=b.sm_scale, workspace=ws,
                                device_error=self.err, **kw)
@@ -153,3 +156,12 @@ def prefill_chunks(b: W.Batch, chunk: int):
         toks = np.concatenate([qo[i] + done[i] + np.arange(ext[i]) for i in range(E.size)]).astype(np.int64)
         yield (b.ext_q[toks], (P + done).astype(np.int32), ext,
                np.concatenate([[0], np.cumsum(ext)]).astype(np.int32), toks)
+
+
+def attach_tree_groups_multilevel(b: W.Batch) -> W.Batch:
+    """Give a decode batch the multi-level cascade groups of its table rows' tree (one per shared node)."""
+    from prefix_shared_kv_ra_gb300.radix import cascade_groups_multilevel
+    rows = [b.req_to_token[r, :L] for r, L in zip(b.dec_rpi, b.dec_seq_lens)]
+    (b.casc_group_indptr, b.casc_group_reqs, b.casc_group_start, b.casc_group_prefix_len, b.casc_group_level,
+     b.casc_levels) = cascade_groups_multilevel(rows)
+    return b

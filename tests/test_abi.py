@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert ra.ra_abi_version() == 2
+    assert ra.ra_abi_version() == 3
     assert lib.ra_status_string(0) == b"ok"
     assert lib.ra_status_string(3) == b"workspace too small"
 
@@ -53,8 +53,8 @@ FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
 
 def _decode_call(lib, **over):
     args = dict(k=FAKE, v=FAKE, S=1024, hkv=8, d=128, q=FAKE, o=FAKE, hq=32, scale=0.088, table=FAKE,
-                stride=4096, rows=64, rpi=FAKE, lens=FAKE, batch=4, max_len=4096, ng=0, gi=None, gr=None, gp=None,
-                mgp=0, mgs=0, ws=FAKE, wsb=1 << 30, err=None, stream=None)
+                stride=4096, rows=64, rpi=FAKE, lens=FAKE, batch=4, max_len=4096, ng=0, gi=None, gr=None, gs=None,
+                gp=None, gl=None, mgp=0, mgs=0, mgl=1, ws=FAKE, wsb=1 << 30, err=None, stream=None)
     args.update(over)
     return lib.ra_decode_attention(*args.values())
 
@@ -70,6 +70,8 @@ def test_decode_validation(lib):
     assert _decode_call(lib, scale=float("nan")) == 1
     assert _decode_call(lib, batch=-1) == 1
     assert _decode_call(lib, ng=2, gi=None) == 1               # cascade arrays missing
+    assert _decode_call(lib, ng=2, gi=FAKE, gr=FAKE, gp=FAKE, mgp=100, mgs=2, mgl=2) == 1  # levels need group_level
+    assert _decode_call(lib, ng=2, gi=FAKE, gr=FAKE, gp=FAKE, mgp=100, mgs=2, mgl=0) == 1  # no level
     assert _decode_call(lib, batch=0) == 0                     # empty batch: no-op
 
 
@@ -77,6 +79,8 @@ def test_decode_workspace_grows_with_bounds(lib):
     a = ra.ra_decode_workspace_bytes(64, 32, 8, 128, 4096)
     b = ra.ra_decode_workspace_bytes(64, 32, 8, 128, 512)
     c = ra.ra_decode_workspace_bytes(64, 32, 8, 128, 4096, 8, 1024, 8)
+    c3 = ra.ra_decode_workspace_bytes(64, 32, 8, 128, 4096, 8, 1024, 8, 3)
+    assert c3 > c  # three levels of prefix partials
     d = ra.ra_decode_workspace_bytes(64, 32, 8, 128, 32768)
     assert 0 < b < a < c and d >= a
     assert ra.ra_decode_workspace_bytes(0, 32, 8, 128, 4096) == 0

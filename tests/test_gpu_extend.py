@@ -7,7 +7,8 @@ import torch
 import oracle
 import prefix_shared_kv_ra_gb300 as ra
 import workloads as W
-from helpers import DeviceBatch, assert_close, attach_tree_groups, grow_key_scale, prefill_chunks, to_f64
+from helpers import (DeviceBatch, assert_close, attach_tree_groups, attach_tree_groups_multilevel, grow_key_scale,
+                     prefill_chunks, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -219,3 +220,24 @@ def test_cascade_growing_scores():
     db = DeviceBatch(b)
     db.store()
     check_cascade(db)
+
+
+@pytest.mark.parametrize("seed,hq,hkv,d", [(51, 32, 8, 128), (52, 16, 2, 64)])
+def test_cascade_multilevel_random(seed, hq, hkv, d):
+    """One group per shared node of the decode rows' tree: nested ranges at several levels."""
+    b = attach_tree_groups_multilevel(W.random_mixed(seed, n_extend=0, n_decode=24, num_q_heads=hq, num_kv_heads=hkv,
+                                                     head_dim=d, max_len=1200, min_len=200, share_prob=0.95))
+    assert b.has_cascade() and b.casc_levels >= 2
+    db = DeviceBatch(b)
+    db.store()
+    check_cascade(db)
+
+
+def test_cascade_multilevel_multiturn_mix_sampled():
+    b = attach_tree_groups_multilevel(W.cfg5_multiturn_mix_70b())
+    assert b.casc_levels >= 2
+    db = DeviceBatch(b)
+    db.store()
+    rng = np.random.default_rng(8)
+    n = b.n_decode * b.num_q_heads
+    check_cascade(db, sel=np.sort(rng.choice(n, 512, replace=False)))

@@ -182,3 +182,55 @@ def test_evictable_size_tracks_locks_inserts_and_evictions():
         else:
             cache.evict(int(rng.integers(1, 40)))
         assert cache.evictable_size == brute(), step
+
+
+def test_multilevel_groups_are_the_shared_nodes_of_the_rows():
+    # rows (slot sequences): a, b share 0..5; c shares 0..2 with them; d is alone
+    base = list(range(100, 106))
+    rows = [base + [1, 2, 3], base + [7, 8], base[:3] + [40, 41, 42, 43], [900, 901, 902]]
+    from prefix_shared_kv_ra_gb300.radix import cascade_groups_multilevel
+    indptr, reqs, start, end, level, nl = cascade_groups_multilevel(rows)
+    groups = {(int(s), int(e), int(l)): sorted(reqs[indptr[g]:indptr[g + 1]].tolist())
+              for g, (s, e, l) in enumerate(zip(start, end, level))}
+    assert groups == {(0, 3, 0): [0, 1, 2], (3, 6, 1): [0, 1]} and nl == 2
+    # every request's groups cover 0 .. (deepest end) - 1 without gaps, members share the slots, and the
+    # newest token stays private
+    for b, row in enumerate(rows):
+        mine = sorted((s, e) for (s, e, l), m in groups.items() if b in m)
+        pos = 0
+        for s, e in mine:
+            assert s == pos
+            pos = e
+        assert pos <= len(row) - 1
+    for (s, e, l), m in groups.items():
+        for b in m:
+            assert rows[b][s:e] == rows[m[0]][s:e]
+
+
+def test_multilevel_groups_on_a_generated_batch():
+    from prefix_shared_kv_ra_gb300.radix import cascade_groups_multilevel
+    b = W.cfg5_multiturn_mix_70b()
+    rows = [b.req_to_token[r, :L] for r, L in zip(b.dec_rpi, b.dec_seq_lens)]
+    indptr, reqs, start, end, level, nl = cascade_groups_multilevel(rows)
+    assert nl >= 2 and len(start) > 0
+    cover = {}
+    for g in range(len(start)):
+        for m in reqs[indptr[g]:indptr[g + 1]]:
+            cover.setdefault(int(m), []).append((int(start[g]), int(end[g]), int(level[g])))
+            assert np.array_equal(rows[m][start[g]:end[g]], rows[reqs[indptr[g]]][start[g]:end[g]])
+    for m, rng in cover.items():
+        rng.sort()
+        assert [l for _, _, l in rng] == list(range(len(rng)))   # one group per level, in depth order
+        assert rng[0][0] == 0 and all(rng[i][1] == rng[i + 1][0] for i in range(len(rng) - 1))
+        assert rng[-1][1] <= len(rows[m]) - 1
+
+
+def test_multilevel_short_nodes_fold_into_the_groups_below():
+    from prefix_shared_kv_ra_gb300.radix import cascade_groups_multilevel
+    base = list(range(100, 106))
+    rows = [base + [1, 2, 3], base + [7, 8], base[:3] + [40, 41, 42, 43], [900, 901, 902]]
+    indptr, reqs, start, end, level, nl = cascade_groups_multilevel(rows, min_range=4)
+    groups = {(int(s), int(e), int(l)): sorted(reqs[indptr[g]:indptr[g + 1]].tolist())
+              for g, (s, e, l) in enumerate(zip(start, end, level))}
+    # the 3-token node shared by rows 0-2 is too short: its positions join the node below (rows 0, 1)
+    assert groups == {(0, 6, 0): [0, 1]} and nl == 1

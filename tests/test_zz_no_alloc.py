@@ -42,7 +42,8 @@ def _static_call(db: DeviceBatch, cascade: bool, out: torch.Tensor) -> int:
     return lib.ra_decode_attention_static(
         ptr(db.k_pool), ptr(db.v_pool), b.num_slots, b.num_kv_heads, b.head_dim, ptr(db.dec_q), ptr(out),
         b.num_q_heads, b.sm_scale, ptr(db.table), db.table.shape[1], db.table.shape[0], ptr(db.dec_rpi),
-        ptr(db.dec_lens), b.n_decode, b.max_seq_len, ng, ptr(gi), ptr(gr), ptr(gp), mgp, mgs, ptr(db.err), stream)
+        ptr(db.dec_lens), b.n_decode, b.max_seq_len, ng, ptr(gi), ptr(gr), None, ptr(gp), None, mgp, mgs, 1,
+        ptr(db.err), stream)
 
 
 def _reference(db: DeviceBatch, cascade: bool) -> np.ndarray:
@@ -87,7 +88,7 @@ def test_static_scratch_decode_rejects_sizes_beyond_the_array():
     st = lib.ra_decode_attention_static(
         P(db.k_pool.data_ptr()), P(db.v_pool.data_ptr()), b.num_slots, 8, 128, P(db.dec_q.data_ptr()),
         P(out.data_ptr()), 64, b.sm_scale, P(db.table.data_ptr()), 32768, db.table.shape[0],
-        P(db.dec_rpi.data_ptr()), P(db.dec_lens.data_ptr()), 224, 32768, 0, None, None, None, 0, 0, None,
-        P(torch.cuda.current_stream(db.dev).cuda_stream))
+        P(db.dec_rpi.data_ptr()), P(db.dec_lens.data_ptr()), 224, 32768, 0, None, None, None, None, None, 0, 0, 1,
+        None, P(torch.cuda.current_stream(db.dev).cuda_stream))
     assert st == 3  # RA_ERR_WORKSPACE, nothing launched
     assert b"static scratch" in lib.ra_last_error_message()

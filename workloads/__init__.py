@@ -110,10 +110,13 @@ class Batch:
     dec_rpi: np.ndarray             # int32 [Bd]
     dec_seq_lens: np.ndarray        # int32 [Bd] (includes the new token)
     dec_q: np.ndarray               # uint16 [Bd, Hq, D]
-    # optional one-level cascade over decode requests
+    # optional cascade over decode requests: group g covers positions [start, prefix_len) of its members
     casc_group_indptr: Optional[np.ndarray] = None   # int32 [NG + 1]
     casc_group_reqs: Optional[np.ndarray] = None     # int32 [sum members] (decode batch indices)
-    casc_group_prefix_len: Optional[np.ndarray] = None  # int32 [NG]
+    casc_group_prefix_len: Optional[np.ndarray] = None  # int32 [NG] (range end)
+    casc_group_start: Optional[np.ndarray] = None    # int32 [NG]; None = all 0 (one level)
+    casc_group_level: Optional[np.ndarray] = None    # int32 [NG]; None = all 0
+    casc_levels: int = 1
     # cached token ids of every sequence in build order (for hit-ratio checks)
     tokens: List[np.ndarray] = field(default_factory=list)
     specs: List[SeqSpec] = field(default_factory=list)
