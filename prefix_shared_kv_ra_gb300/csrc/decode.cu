@@ -374,12 +374,15 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
 }
 
 // Merge the partials of every request that has more than one (the shared-prefix pass's and the
-// private splits'): o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M).  One warp per (request, q head);
-// lanes load the log-sum-exps 32 at a time (split base + k on lane k), reduce the maximum and the
-// weights with shuffles, then stream the partial rows with independent loads, each lane owning D/32 dims.
+// private splits'): o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M).  One warp per (request, q head),
+// each lane owning D/32 dims.  The merge is latency-bound, so a warp keeps its loads in flight together:
+// the log-sum-exps of 32 splits (one per lane) and the first kRows partial rows are issued at once, the
+// weights follow from warp shuffles, and further rows come kRows at a time.  Chunks of 32 splits are
+// folded with a running maximum.
 template <int D>
 __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
   constexpr int V = D / 32;
+  constexpr int kRows = 16;
   griddep_wait();  // the decode kernel (and, through it, the prefix pass) has completed
   griddep_launch();
   const int warp_global = blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -401,28 +404,56 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
   auto lse_of = [&](int s) {
     return s < n_pre ? p.casc_lse[bh * p.casc_slots + s] : p.part_lse[bh * p.max_splits + (s - n_pre)];
   };
-  float mm = -INFINITY;
-  for (int base = 0; base < n; base += 32)
-    if (base + lane < n) mm = fmaxf(mm, lse_of(base + lane));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
+  auto load_row = [&](int s, float (&x)[V]) {
+    const float* src = (s < n_pre ? p.casc_o + (bh * p.casc_slots + s) * D
+                                  : p.part_o + (bh * p.max_splits + (s - n_pre)) * D) + lane * V;
+    if constexpr (V == 4) {
+      const float4 t = *reinterpret_cast<const float4*>(src);
+      x[0] = t.x, x[1] = t.y, x[2] = t.z, x[3] = t.w;
+    } else {
+      const float2 t = *reinterpret_cast<const float2*>(src);
+      x[0] = t.x, x[1] = t.y;
+    }
+  };
   float acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
-  float wsum = 0.f;
+  float mrun = -INFINITY, wsum = 0.f;  // wsum: this lane's splits' weights (relative to mrun)
   for (int base = 0; base < n; base += 32) {
     const int cnt = n - base < 32 ? n - base : 32;
-    const float wl = lane < cnt ? ex2(lse_of(base + lane) - mm) : 0.f;  // weight of split base + lane
-    wsum += wl;
-#pragma unroll 4
-    for (int k = 0; k < cnt; ++k) {
-      const int s = base + k;
-      const float w = __shfl_sync(0xffffffffu, wl, k);
-      if (w == 0.f) continue;  // an empty prefix slot (its partial was never written)
-      const float* src = s < n_pre ? p.casc_o + (bh * p.casc_slots + s) * D
-                                   : p.part_o + (bh * p.max_splits + (s - n_pre)) * D;
+    const float ls = lane < cnt ? lse_of(base + lane) : -INFINITY;
+    float x[kRows][V];
 #pragma unroll
-      for (int v = 0; v < V; ++v) acc[v] += w * src[lane * V + v];
+    for (int k = 0; k < kRows; ++k)
+      if (k < cnt) load_row(base + k, x[k]);
+    float mc = ls;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, off));
+    const float mnew = fmaxf(mrun, mc);
+    if (mnew == -INFINITY) continue;  // no partial written so far
+    const float sc = ex2(mrun - mnew);  // 0 while mrun is -inf (acc and wsum are 0 then)
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] *= sc;
+    wsum *= sc;
+    mrun = mnew;
+    const float wl = ex2(ls - mnew);  // weight of split base + lane (0 for an empty slot)
+    wsum += wl;
+    for (int k0 = 0; k0 < cnt; k0 += kRows) {
+      if (k0 > 0) {
+#pragma unroll
+        for (int k = 0; k < kRows; ++k)
+          if (k0 + k < cnt) load_row(base + k0 + k, x[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < kRows; ++k) {
+        if (k0 + k < cnt) {
+          const float w = __shfl_sync(0xffffffffu, wl, k0 + k);
+          if (w > 0.f) {  // an empty prefix slot (never written) has weight 0 and is skipped
+#pragma unroll
+            for (int v = 0; v < V; ++v) acc[v] = fmaf(w, x[k][v], acc[v]);
+          }
+        }
+      }
     }
   }
 #pragma unroll
