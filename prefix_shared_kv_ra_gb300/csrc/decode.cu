@@ -102,9 +102,10 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
   const uint32_t item0 = sbase + 256;  // kItemRing mbarriers: entry published
   const uint32_t stage0 = sbase + kHdrBytes;
   const int RS = p.row_stride;
-  // Let the combine launch; this kernel reads nothing its predecessor (the cascade prefix pass, which
-  // only writes prefix partials) produces, so it does not wait for it here.  It waits before leaving,
-  // so that its completion implies the prefix pass's (the combine reads both).
+  // Let the combine launch.  With groups this kernel reads nothing its predecessor (the cascade prefix
+  // pass, which only writes prefix partials) produces, so it does not wait for it here; without them
+  // the producers wait for the counter-zeroing kernel before the first claim.  It waits before
+  // leaving, so that its completion implies the prefix pass's (the combine reads both).
   griddep_launch();
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s) {
@@ -161,6 +162,9 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
       key = key < nk ? key : nk - 1;
       return __ldg(p.table + static_cast<int64_t>(it.row) * p.table_stride + it.k0 + key);
     };
+    // without groups the previous kernel is the one that zeroes the work counter: wait for it (with
+    // groups it completed before the prefix pass started, which launched this kernel)
+    if (p.key_start == nullptr) griddep_wait();
     if (leader) publish(0, claim());
     int32_t n = 0, c = 0, s = 0;
     Item it;
@@ -465,6 +469,13 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
         __floats2bfloat162_rn(acc[v] * inv, acc[v + 1] * inv);
 }
 
+// Zero the workspace's integer block (work counters, key starts) at the head of the call.
+__global__ void zero_ints_kernel(int32_t* x, int32_t n) {
+  griddep_wait();  // earlier kernels on the stream may still use the workspace
+  griddep_launch();
+  for (int32_t i = threadIdx.x; i < n; i += blockDim.x) x[i] = 0;
+}
+
 // key_start[b] = the largest range end of b's cascade groups (0 for requests in no group, set by the
 // memset); every prefix-partial slot's log-sum-exp starts at -inf (slots no group writes stay so).
 __global__ void cascade_key_start_kernel(int32_t* key_start, int32_t batch, const int32_t* group_indptr,
@@ -685,8 +696,10 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
   int32_t* ints = reinterpret_cast<int32_t*>(ws + wl.ints);
   p.counter = ints + batch;
   p.prefix_counter = ints + batch + 1;
-  cudaError_t e = cudaMemsetAsync(ints, 0, wl.ints_bytes, s);
-  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+  // a kernel rather than a memset, so that the launches of the call stay chained programmatically
+  if (ra_status st = launch_pdl("zero_ints_kernel", zero_ints_kernel, dim3(1), dim3(256), 0, s, ints,
+                                static_cast<int32_t>(wl.ints_bytes / sizeof(int32_t))))
+    return st;
   if (num_groups > 0) {
     p.cchunk = pl.cchunk;
     p.max_csplits = pl.max_csplits;
