@@ -38,45 +38,39 @@ namespace ra {
 namespace {
 
 constexpr int kSlab = 16;          // keys per ring stage (the MMA M side)
-constexpr int kMaxChunk = 1024;    // keys per item (plan_decode never exceeds it)
 constexpr int kMaxStages = 8;
 constexpr int kItemRing = 16;      // published items; the leader runs at most nstage + 1 items ahead
 constexpr int kProducers = 4;      // warps issuing the bulk copies of a slab (TMA issue rate grows with them)
 constexpr int kRowsPerProducer = 2 * kSlab / kProducers;  // K rows then V rows of a slab, split evenly
 constexpr int kHdrBytes = 512;     // full/empty barriers, item ring, abort flag, item barriers
 constexpr int kSmemLimit = 227 * 1024;
+constexpr int kPlanThreads = 1024;  // one CTA plans the call
+constexpr int kRemBuckets = 64;     // size classes of the requests' last (short) items
+constexpr int kCombineWarps = 4;    // (request, q head) merges per combine CTA
 
-// One work item: keys [k0, k1) of request b for the kv heads of head group hg.
+// One work item: keys [k0, k1) of request b for the kv heads of head group hg; d is its dense index
+// (request-major: the item's partial results live at d).
 struct Item {
-  int32_t b, split, hg, k0, k1, start, n_splits, row;
+  int32_t b, split, hg, k0, k1, start, n_splits, row, d;
 };
 
-// Item `idx` = (b * max_splits + split) * n_hgroups + hg: request-major, so the empty splits of a
-// request (split >= its split count) are one contiguous run the producer can skip at once, and
-// requests next to each other (often sharing a prefix) are in flight together. False if empty.
-__device__ __forceinline__ bool decode_item(const DecodeParams& p, int32_t idx, Item& it, bool report) {
+// Claim `idx` = (position in the plan's longest-first order) * n_hgroups + hg.  The plan (written by
+// decode_plan_kernel) lists only non-empty items of valid requests.  Plan arrays are read with plain
+// loads: they are written on the device by the kernel before this one.
+__device__ __forceinline__ void decode_item(const DecodeParams& p, int32_t idx, Item& it) {
   it.hg = idx % p.n_hgroups;
-  const int32_t t = idx / p.n_hgroups;
-  it.split = t % p.max_splits;
-  it.b = t / p.max_splits;
-  int32_t L = __ldg(p.seq_lens + it.b);
+  it.d = p.order[idx / p.n_hgroups];
+  it.b = p.item_req[it.d];
+  const int32_t i0 = p.req_item0[it.b];
+  it.split = it.d - i0;
+  it.n_splits = p.req_item0[it.b + 1] - i0;
   it.row = __ldg(p.rpi + it.b);
-  const bool first = report && it.split == 0 && it.hg == 0;
-  if (it.row < 0 || it.row >= p.table_rows || L < 1) {
-    if (first) flag_error(p.err, (it.row < 0 || it.row >= p.table_rows) ? RA_DEVERR_TABLE : RA_DEVERR_LENGTH);
-    return false;
-  }
-  if (L > p.max_seq_len) {
-    if (first) flag_error(p.err, RA_DEVERR_LENGTH);
-    L = p.max_seq_len;
-  }
-  int32_t start = p.key_start ? __ldg(p.key_start + it.b) : 0;
+  const int32_t L = min(__ldg(p.seq_lens + it.b), p.max_seq_len);
+  const int32_t start = p.key_start ? __ldg(p.key_start + it.b) : 0;
   it.start = start < 0 ? 0 : (start > L ? L : start);
-  it.n_splits = (L - it.start + p.chunk - 1) / p.chunk;
-  if (it.split >= it.n_splits) return false;
-  it.k0 = it.start + it.split * p.chunk;
-  it.k1 = min(L, it.k0 + p.chunk);
-  return true;
+  const int32_t chunk = p.plan[1];
+  it.k0 = it.start + it.split * chunk;
+  it.k1 = min(L, it.k0 + chunk);
 }
 
 // Persistent split-KV decode.  One CTA per SM pulls (request, split, head group) items from a
@@ -102,10 +96,11 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
   const uint32_t item0 = sbase + 256;  // kItemRing mbarriers: entry published
   const uint32_t stage0 = sbase + kHdrBytes;
   const int RS = p.row_stride;
-  // Let the combine launch.  With groups this kernel reads nothing its predecessor (the cascade prefix
-  // pass, which only writes prefix partials) produces, so it does not wait for it here; without them
-  // the producers wait for the counter-zeroing kernel before the first claim.  It waits before
-  // leaving, so that its completion implies the prefix pass's (the combine reads both).
+  // Let the combine launch.  Without groups the producers and consumers wait for the plan kernel before
+  // the first claim.  With groups the plan kernel made its writes visible before it let this kernel
+  // launch, and it completes only after the prefix pass: this kernel reads nothing the pass writes, so
+  // it does not wait here (it runs beside the pass).  It waits before leaving, so that its completion
+  // implies the plan's and the prefix pass's (the combine reads both passes' partials).
   griddep_launch();
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s) {
@@ -128,18 +123,12 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
     const int key_in_slab = row_id & (kSlab - 1);
     const __nv_bfloat16* pool = is_v ? p.v_pool : p.k_pool;
     const uint32_t row_off = (is_v ? kSlab * RS : 0) + key_in_slab * RS;
+    int32_t n_claims = 0;  // plan items x head groups (read once the plan is visible)
     auto claim = [&]() -> int32_t {  // warp-collective
-      for (;;) {
-        int32_t idx = 0;
-        if (lane == 0) idx = atomicAdd(p.counter, 1);
-        idx = __shfl_sync(0xffffffffu, idx, 0);
-        if (idx >= p.n_items) return -1;
-        Item it;
-        if (decode_item(p, idx, it, lane == 0)) return idx;
-        // the rest of this request's items are empty too: move everyone past them
-        const int32_t per_req = p.max_splits * p.n_hgroups;
-        if (lane == 0) atomicMax(p.counter, (idx / per_req + 1) * per_req);
-      }
+      int32_t idx = 0;
+      if (lane == 0) idx = atomicAdd(p.counter, 1);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      return idx < n_claims ? idx : -1;
     };
     auto publish = [&](int32_t n, int32_t idx) {
       if (lane == 0) {
@@ -152,7 +141,7 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
       if (!mbar_wait(item0 + 8 * (n % kItemRing), (n / kItemRing) & 1)) return -1;
       const int32_t idx = s_items[n % kItemRing];
       if (idx < 0) return 0;
-      decode_item(p, idx, it, false);
+      decode_item(p, idx, it);
       return 1;
     };
     auto load_slot = [&](const Item& it, int32_t s) -> int32_t {  // rows past the range repeat the last key
@@ -162,9 +151,10 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
       key = key < nk ? key : nk - 1;
       return __ldg(p.table + static_cast<int64_t>(it.row) * p.table_stride + it.k0 + key);
     };
-    // without groups the previous kernel is the one that zeroes the work counter: wait for it (with
-    // groups it completed before the prefix pass started, which launched this kernel)
+    // without groups the plan (and the reset work counter) is visible once the plan kernel completes;
+    // with groups it was made visible before this kernel launched
     if (p.key_start == nullptr) griddep_wait();
+    n_claims = p.plan[0] * p.n_hgroups;
     if (leader) publish(0, claim());
     int32_t n = 0, c = 0, s = 0;
     Item it;
@@ -235,6 +225,7 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
   }
 
   // ================================================================ consumers
+  if (p.key_start == nullptr) griddep_wait();  // the plan the items are decoded from is visible
   const int g = lane >> 2;  // q head within the GQA group (MMA N index)
   const int tq = lane & 3;
   const uint32_t a_off = (lane & 15) * RS + (lane >> 4) * 16 + warp * D * 2;
@@ -250,7 +241,7 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
       break;
     }
     Item it;
-    decode_item(p, idx, it, false);
+    decode_item(p, idx, it);
     const int kh = it.hg * p.hpc + warp;
     // Q^T fragments (B operand): column g is q head kh*G + g
     uint32_t qf[KT][2];
@@ -349,8 +340,8 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
         }
       }
     } else {
-      const int64_t ps0 = bh0 * p.max_splits + it.split;
-      const int64_t ps1 = ps0 + p.max_splits;
+      const int64_t ps0 = static_cast<int64_t>(it.d) * p.hq + kh * p.group + 2 * tq;  // partial row of (item, head)
+      const int64_t ps1 = ps0 + 1;
 #pragma unroll
       for (int mt = 0; mt < KT; ++mt) {
         const int d = mt * 16 + g;
@@ -377,19 +368,21 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
   griddep_wait();
 }
 
-// Merge the partials of every request that has more than one (the shared-prefix pass's and the
-// private splits'): o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M).  One warp per (request, q head),
-// each lane owning D/32 dims.  The merge is latency-bound, so a warp keeps its loads in flight together:
-// the log-sum-exps of 32 splits (one per lane) and the first kRows partial rows are issued at once, the
-// weights follow from warp shuffles, and further rows come kRows at a time.  Chunks of 32 splits are
-// folded with a running maximum.
+// Merge the partials of every request that has more than one (its private splits' and the shared-prefix
+// pass's): o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M).  One warp per (request, q head), each lane
+// owning D/32 dims.  The merge is latency-bound, so a warp keeps its loads in flight together: the
+// log-sum-exps of 32 partials (one per lane) and the first kRows private partial rows are issued at once
+// (private partials are always written), the weights follow from warp shuffles, and the other rows come
+// kRows at a time, prefix rows only where a group wrote them (a finite log-sum-exp; most of the prefix
+// slots of a request are empty).  Partials are taken private first, then prefix, in chunks of 32 folded
+// with a running maximum.
 template <int D>
-__global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(32 * kCombineWarps) decode_combine_kernel(const DecodeParams p) {
   constexpr int V = D / 32;
-  constexpr int kRows = 16;
+  constexpr int kRows = 8;
   griddep_wait();  // the decode kernel (and, through it, the prefix pass) has completed
   griddep_launch();
-  const int warp_global = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int warp_global = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (warp_global >= p.batch * p.hq) return;
   const int b = warp_global / p.hq;
@@ -399,18 +392,20 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
   if (L > p.max_seq_len) L = p.max_seq_len;
   int32_t start = p.key_start ? __ldg(p.key_start + b) : 0;
   start = start < 0 ? 0 : (start > L ? L : start);
-  const int32_t n_splits = (L - start + p.chunk - 1) / p.chunk;
+  const int32_t i0 = p.req_item0[b];  // the request's private items are i0 .. i0 + n_splits - 1
+  const int32_t n_splits = p.req_item0[b + 1] - i0;
   // prefix partials: every slot of every level; those no group wrote hold -inf (weight 0, skipped)
   const int32_t n_pre = start > 0 ? p.casc_slots : 0;
   if (n_splits == 1 && n_pre == 0) return;  // written directly by the decode kernel
-  const int32_t n = n_pre + n_splits;
+  const int32_t n = n_splits + n_pre;
   const int64_t bh = warp_global;
+  const int64_t h = bh - static_cast<int64_t>(b) * p.hq;
   auto lse_of = [&](int s) {
-    return s < n_pre ? p.casc_lse[bh * p.casc_slots + s] : p.part_lse[bh * p.max_splits + (s - n_pre)];
+    return s < n_splits ? p.part_lse[(i0 + s) * p.hq + h] : p.casc_lse[bh * p.casc_slots + (s - n_splits)];
   };
   auto load_row = [&](int s, float (&x)[V]) {
-    const float* src = (s < n_pre ? p.casc_o + (bh * p.casc_slots + s) * D
-                                  : p.part_o + (bh * p.max_splits + (s - n_pre)) * D) + lane * V;
+    const float* src = (s < n_splits ? p.part_o + ((i0 + s) * p.hq + h) * D
+                                     : p.casc_o + (bh * p.casc_slots + (s - n_splits)) * D) + lane * V;
     if constexpr (V == 4) {
       const float4 t = *reinterpret_cast<const float4*>(src);
       x[0] = t.x, x[1] = t.y, x[2] = t.z, x[3] = t.w;
@@ -422,14 +417,14 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
   float acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
-  float mrun = -INFINITY, wsum = 0.f;  // wsum: this lane's splits' weights (relative to mrun)
+  float mrun = -INFINITY, wsum = 0.f;  // wsum: this lane's partials' weights (relative to mrun)
   for (int base = 0; base < n; base += 32) {
     const int cnt = n - base < 32 ? n - base : 32;
     const float ls = lane < cnt ? lse_of(base + lane) : -INFINITY;
     float x[kRows][V];
 #pragma unroll
     for (int k = 0; k < kRows; ++k)
-      if (k < cnt) load_row(base + k, x[k]);
+      if (k < cnt && base + k < n_splits) load_row(base + k, x[k]);  // private: written, load at once
     float mc = ls;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, off));
@@ -440,22 +435,22 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
     for (int v = 0; v < V; ++v) acc[v] *= sc;
     wsum *= sc;
     mrun = mnew;
-    const float wl = ex2(ls - mnew);  // weight of split base + lane (0 for an empty slot)
+    const float wl = ex2(ls - mnew);  // weight of partial base + lane (0 for an empty prefix slot)
     wsum += wl;
     for (int k0 = 0; k0 < cnt; k0 += kRows) {
-      if (k0 > 0) {
 #pragma unroll
-        for (int k = 0; k < kRows; ++k)
-          if (k0 + k < cnt) load_row(base + k0 + k, x[k]);
+      for (int k = 0; k < kRows; ++k) {
+        const int s = base + k0 + k;
+        const bool loaded = k0 == 0 && s < n_splits;
+        const float w = __shfl_sync(0xffffffffu, wl, (k0 + k) & 31);
+        if (k0 + k < cnt && w > 0.f && !loaded) load_row(s, x[k]);
       }
 #pragma unroll
       for (int k = 0; k < kRows; ++k) {
-        if (k0 + k < cnt) {
-          const float w = __shfl_sync(0xffffffffu, wl, k0 + k);
-          if (w > 0.f) {  // an empty prefix slot (never written) has weight 0 and is skipped
+        const float w = __shfl_sync(0xffffffffu, wl, (k0 + k) & 31);
+        if (k0 + k < cnt && w > 0.f) {
 #pragma unroll
-            for (int v = 0; v < V; ++v) acc[v] = fmaf(w, x[k][v], acc[v]);
-          }
+          for (int v = 0; v < V; ++v) acc[v] = fmaf(w, x[k][v], acc[v]);
         }
       }
     }
@@ -467,6 +462,134 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const DecodeParams 
   for (int v = 0; v < V; v += 2)
     *reinterpret_cast<__nv_bfloat162*>(p.o + bh * D + lane * V + v) =
         __floats2bfloat162_rn(acc[v] * inv, acc[v + 1] * inv);
+}
+
+// Block-wide exclusive scan of (a, b) pairs over kPlanThreads threads; totals returned in ta, tb.
+__device__ __forceinline__ void plan_scan2(int32_t& a, int32_t& b, int32_t& ta, int32_t& tb, int32_t* s_wa,
+                                           int32_t* s_wb) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int32_t ia = a, ib = b;  // inclusive within the warp
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t xa = __shfl_up_sync(0xffffffffu, ia, off), xb = __shfl_up_sync(0xffffffffu, ib, off);
+    if (lane >= off) ia += xa, ib += xb;
+  }
+  if (lane == 31) s_wa[warp] = ia, s_wb[warp] = ib;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t wa = s_wa[lane], wb = s_wb[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t xa = __shfl_up_sync(0xffffffffu, wa, off), xb = __shfl_up_sync(0xffffffffu, wb, off);
+      if (lane >= off) wa += xa, wb += xb;
+    }
+    s_wa[lane] = wa, s_wb[lane] = wb;  // inclusive warp totals
+  }
+  __syncthreads();
+  const int32_t pa = warp > 0 ? s_wa[warp - 1] : 0, pb = warp > 0 ? s_wb[warp - 1] : 0;
+  ta = s_wa[31], tb = s_wb[31];
+  a = pa + ia - a;
+  b = pb + ib - b;
+  __syncthreads();  // the scratch may be reused
+}
+
+// The private-key work plan of one decode call, made on the device from the real lengths (the host only
+// knows bounds).  T = the batch's private keys (seq_len minus the cascade start, over valid requests);
+// chunk = max(kDecodeMinChunk, T / kDecodePlanItems rounded up to 16), so a call has at most
+// kDecodePlanItems + batch items however long its contexts are.  Request b's items get the dense indices
+// req_item0[b] .. req_item0[b+1]-1 (where their partials live); the claim order lists every full-chunk
+// item first, then each request's shorter last item by decreasing size (longest processing time first),
+// so the CTAs that finish last finish on short items.  One CTA of kPlanThreads threads; each thread owns
+// a contiguous run of requests.  It also resets the work counter.
+__global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeParams p) {
+  __shared__ int32_t s_wa[32], s_wb[32];
+  __shared__ int32_t s_hist[kRemBuckets];
+  __shared__ unsigned long long s_total;
+  // Without groups this is the call's first kernel: it waits for earlier kernels (they may still use the
+  // workspace) and lets the decode kernel launch at once (the decode kernel waits for this grid before its
+  // first claim).  With groups it runs behind the prefix pass, which let it launch only after the key
+  // starts were complete; it does not wait for the pass, so that the decode kernel can run beside it.
+  const bool behind_pass = p.key_start != nullptr;
+  if (!behind_pass) {
+    griddep_wait();
+    griddep_launch();
+  }
+  const int t = threadIdx.x;
+  const int32_t per = (p.batch + kPlanThreads - 1) / kPlanThreads;
+  const int32_t r0 = min(p.batch, t * per), r1 = min(p.batch, r0 + per);
+  auto len_of = [&](int32_t b, bool report) -> int32_t {
+    const int32_t row = __ldg(p.rpi + b);
+    int32_t L = __ldg(p.seq_lens + b);
+    if (row < 0 || row >= p.table_rows || L < 1) {
+      if (report) flag_error(p.err, (row < 0 || row >= p.table_rows) ? RA_DEVERR_TABLE : RA_DEVERR_LENGTH);
+      return 0;
+    }
+    if (L > p.max_seq_len) {
+      if (report) flag_error(p.err, RA_DEVERR_LENGTH);
+      L = p.max_seq_len;
+    }
+    int32_t start = p.key_start ? p.key_start[b] : 0;
+    start = start < 0 ? 0 : (start > L ? L : start);
+    return L - start;
+  };
+  if (t == 0) s_total = 0ull;
+  if (t < kRemBuckets) s_hist[t] = 0;
+  __syncthreads();
+  unsigned long long tot = 0;
+  for (int32_t b = r0; b < r1; ++b) tot += static_cast<unsigned long long>(len_of(b, true));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+  if ((t & 31) == 0) atomicAdd(&s_total, tot);
+  __syncthreads();
+  const unsigned long long per_item = (s_total + kDecodePlanItems - 1) / kDecodePlanItems;
+  // (the host bounds batch x max_seq_len by kDecodePlanItems x 2^30, so the chunk fits in 31 bits)
+  const int32_t chunk = static_cast<int32_t>(
+      per_item <= kDecodeMinChunk ? kDecodeMinChunk : ((per_item + 15) / 16) * 16);
+  // item counts (all, full-chunk) of this thread's requests, scanned over the block
+  int32_t cnt = 0, full = 0;
+  for (int32_t b = r0; b < r1; ++b) {
+    const int32_t len = len_of(b, false);
+    cnt += (len + chunk - 1) / chunk;
+    full += len / chunk;
+    const int32_t rem = len % chunk;
+    if (rem > 0) atomicAdd(&s_hist[static_cast<int64_t>(chunk - rem) * kRemBuckets / chunk], 1);
+  }
+  int32_t n_items, n_full;
+  plan_scan2(cnt, full, n_items, n_full, s_wa, s_wb);
+  if (t == 0) {  // bucket starts, largest remainders first, after the full items
+    int32_t acc = n_full;
+    for (int k = 0; k < kRemBuckets; ++k) {
+      const int32_t c = s_hist[k];
+      s_hist[k] = acc;
+      acc += c;
+    }
+  }
+  __syncthreads();
+  for (int32_t b = r0; b < r1; ++b) {
+    const int32_t len = len_of(b, false);
+    const int32_t c = (len + chunk - 1) / chunk, f = len / chunk, rem = len % chunk;
+    p.req_item0[b] = cnt;
+    for (int32_t s = 0; s < c; ++s) p.item_req[cnt + s] = b;
+    for (int32_t s = 0; s < f; ++s) p.order[full + s] = cnt + s;
+    if (rem > 0) p.order[atomicAdd(&s_hist[static_cast<int64_t>(chunk - rem) * kRemBuckets / chunk], 1)] = cnt + f;
+    cnt += c;
+    full += f;
+  }
+  if (t == 0) {
+    p.req_item0[p.batch] = n_items;
+    p.plan[0] = n_items;
+    p.plan[1] = chunk;
+    *p.counter = 0;
+  }
+  if (behind_pass) {
+    // The decode kernel launches once every thread's plan writes are visible device-wide (it reads the
+    // plan without waiting for this grid); this grid completes only after the prefix pass, so that the
+    // decode kernel's completion, and through it the combine, implies the pass's.
+    __threadfence();
+    __syncthreads();
+    griddep_launch();
+    griddep_wait();
+  }
 }
 
 // Zero the workspace's integer block (work counters, key starts) at the head of the call.
@@ -517,7 +640,8 @@ ra_status launch_decode(const DecodeParams& p, int grid, int smem, cudaStream_t 
   if (ra_status st = launch_pdl("decode_kernel", kern, dim3(grid), dim3(32 * (p.hpc + kProducers)), smem, stream, p))
     return st;
   const int nwarps = p.batch * p.hq;
-  return launch_pdl("decode_combine_kernel", decode_combine_kernel<D>, dim3((nwarps + 3) / 4), dim3(128), 0, stream, p);
+  return launch_pdl("decode_combine_kernel", decode_combine_kernel<D>, dim3((nwarps + kCombineWarps - 1) / kCombineWarps),
+                    dim3(32 * kCombineWarps), 0, stream, p);
 }
 
 }  // namespace
@@ -529,23 +653,15 @@ static int32_t heads_per_cta(int32_t num_kv_heads) {
   return 1;
 }
 
-// Private keys per work item: between 256 and 1024, aiming at ~1K (request, split, head group)
-// items over the host-side bound of the batch's keys.
+// Private keys are cut into items on the device (decode_plan_kernel); the host only bounds their number.
 // Shared-prefix pass (cascade): 256-row items of (member, q head) per group and kv head, each covering
 // at most `cchunk` prefix keys.  The persistent private decode is launched programmatically after it
 // and runs on the SMs the prefix pass leaves free.
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seq_len,
                        int32_t num_groups, int32_t max_group_prefix_len, int32_t max_group_size) {
   DecodePlan pl;
-  const int64_t n_hg = num_kv_heads / heads_per_cta(num_kv_heads);
-  const int64_t work = static_cast<int64_t>(batch) * n_hg * (max_seq_len > 0 ? max_seq_len : 1);
-  int64_t chunk = (work + 1023) / 1024;
-  chunk = (chunk + 63) / 64 * 64;
-  if (chunk < 256) chunk = 256;
-  if (chunk > kMaxChunk) chunk = kMaxChunk;
-  pl.chunk = static_cast<int32_t>(chunk);
-  pl.max_splits = static_cast<int32_t>((static_cast<int64_t>(max_seq_len) + chunk - 1) / chunk);
-  if (pl.max_splits < 1) pl.max_splits = 1;
+  (void)max_seq_len;
+  pl.max_items = kDecodePlanItems + batch;
   if (num_groups > 0 && max_group_prefix_len > 0) {
     // Prefix keys per prefix-pass CTA (a multiple of the 128-key tile, at most 2048): the split count
     // that minimises the pass's makespan, waves x (tiles per CTA + the ~3 tiles' worth of fill and
@@ -582,10 +698,11 @@ DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int3
   DecodeWorkspace w;
   const size_t bh = static_cast<size_t>(batch) * num_q_heads;
   size_t off = 0;
+  const size_t ih = static_cast<size_t>(pl.max_items) * num_q_heads;
   w.part_o = off;
-  off += up(bh * pl.max_splits * head_dim * sizeof(float));
+  off += up(ih * head_dim * sizeof(float));
   w.part_lse = off;
-  off += up(bh * pl.max_splits * sizeof(float));
+  off += up(ih * sizeof(float));
   if (cascade_levels > 0) {
     const size_t slots = static_cast<size_t>(cascade_levels) * pl.max_csplits;
     w.casc_o = off;
@@ -595,7 +712,9 @@ DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int3
   }
   w.ints = off;
   (void)num_kv_heads;
-  w.ints_bytes = (static_cast<size_t>(batch) + 2) * sizeof(int32_t);
+  w.zero_bytes = (static_cast<size_t>(batch) + 2) * sizeof(int32_t);
+  w.ints_bytes = w.zero_bytes + (2 + static_cast<size_t>(batch) + 1 + 2 * static_cast<size_t>(pl.max_items)) *
+                                    sizeof(int32_t);
   off += up(w.ints_bytes);
   w.total = off;
   return w;
@@ -660,6 +779,9 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
                    (!group_prefix_start || aligned4(group_prefix_start)) && (!group_level || aligned4(group_level)),
                "group arrays must be 4-byte aligned");
   }
+  // the device plan's item length must fit in 31 bits (it is at most batch x max_seq_len / kDecodePlanItems)
+  RA_REQUIRE(static_cast<int64_t>(batch) * max_seq_len <= static_cast<int64_t>(kDecodePlanItems) << 30,
+             "batch x max_seq_len too large");
   const DecodePlan pl = plan_decode(batch, num_q_heads, num_kv_heads, max_seq_len, num_groups,
                                     max_group_prefix_len, max_group_size);
   const int32_t levels = num_groups > 0 ? max_group_levels : 0;
@@ -685,8 +807,7 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
   p.seq_lens = seq_lens;
   p.batch = batch;
   p.max_seq_len = max_seq_len;
-  p.chunk = pl.chunk;
-  p.max_splits = pl.max_splits;
+  p.max_items = pl.max_items;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.part_o = reinterpret_cast<float*>(ws + wl.part_o);
   p.part_lse = reinterpret_cast<float*>(ws + wl.part_lse);
@@ -696,10 +817,13 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
   int32_t* ints = reinterpret_cast<int32_t*>(ws + wl.ints);
   p.counter = ints + batch;
   p.prefix_counter = ints + batch + 1;
-  // a kernel rather than a memset, so that the launches of the call stay chained programmatically
-  if (ra_status st = launch_pdl("zero_ints_kernel", zero_ints_kernel, dim3(1), dim3(256), 0, s, ints,
-                                static_cast<int32_t>(wl.ints_bytes / sizeof(int32_t))))
-    return st;
+  p.plan = ints + batch + 2;
+  p.req_item0 = p.plan + 2;
+  p.item_req = p.req_item0 + batch + 1;
+  p.order = p.item_req + pl.max_items;
+  // Kernels rather than memsets, so that the launches of the call stay chained programmatically:
+  // with groups, [zero key starts and counters] -> [key-start scatter] -> [prefix pass] -> [plan] ->
+  // [decode] -> [combine]; without, [plan] -> [decode] -> [combine].
   if (num_groups > 0) {
     p.cchunk = pl.cchunk;
     p.max_csplits = pl.max_csplits;
@@ -707,14 +831,21 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
     p.casc_o = reinterpret_cast<float*>(ws + wl.casc_o);
     p.casc_lse = reinterpret_cast<float*>(ws + wl.casc_lse);
     p.key_start = ints;
+    if (ra_status st = launch_pdl("zero_ints_kernel", zero_ints_kernel, dim3(1), dim3(256), 0, s, ints,
+                                  static_cast<int32_t>(wl.zero_bytes / sizeof(int32_t))))
+      return st;
     if (ra_status st = launch_pdl("cascade_key_start_kernel", cascade_key_start_kernel, dim3((batch + 127) / 128),
                                   dim3(128), 0, s, ints, batch, group_indptr, group_reqs, group_prefix_len, num_groups,
                                   p.casc_lse, static_cast<int64_t>(batch) * num_q_heads * p.casc_slots, device_error))
       return st;
+  }
+  if (num_groups > 0) {
     CascadeArgs ca{group_indptr,         group_reqs,           group_prefix_start, group_prefix_len, group_level,
                    num_groups,           max_group_prefix_len, max_group_size,     max_group_levels};
     if (ra_status st = launch_cascade_prefix(p, ca, head_dim, s)) return st;
   }
+  if (ra_status st = launch_pdl("decode_plan_kernel", decode_plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, p))
+    return st;
   // persistent decode geometry
   p.hpc = heads_per_cta(num_kv_heads);
   p.n_hgroups = num_kv_heads / p.hpc;
@@ -724,9 +855,7 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
   if (p.nstage > kMaxStages) p.nstage = kMaxStages;
   if (p.nstage < 2) return fail(RA_ERR_UNSUPPORTED, "decode ring does not fit in shared memory");
   const int smem = kHdrBytes + p.nstage * p.stage_bytes;
-  const int64_t n_items = static_cast<int64_t>(pl.max_splits) * batch * p.n_hgroups;
-  if (n_items > INT32_MAX / 2) return fail(RA_ERR_UNSUPPORTED, "too many decode work items");
-  p.n_items = static_cast<int32_t>(n_items);
+  const int64_t n_items = static_cast<int64_t>(pl.max_items) * p.n_hgroups;  // bound of the claims
   DeviceInfo dev;
   if (ra_status st = current_device(&dev)) return st;
   const int grid = static_cast<int>(n_items < dev.num_sms ? n_items : dev.num_sms);

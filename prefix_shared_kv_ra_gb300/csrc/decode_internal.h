@@ -31,18 +31,20 @@ struct DecodeParams {
   int32_t batch;
   int32_t max_seq_len;
   const int32_t* key_start;  // [batch] first private position (cascade), or nullptr
-  int32_t chunk;             // keys per split
-  int32_t max_splits;
   int32_t hpc;               // kv heads per CTA item (consumer warps)
   int32_t n_hgroups;         // hkv / hpc
   int32_t nstage;            // ring stages
   int32_t row_stride;        // bytes between keys in a ring stage (hpc * D * 2 + 16)
   int32_t stage_bytes;       // 2 * 16 * row_stride
-  int32_t n_items;           // max_splits * batch * n_hgroups
-  int32_t* counter;          // work-item counter (zeroed before each launch)
-  int32_t* prefix_counter;   // cascade prefix pass's work-item counter (zeroed likewise)
-  float* part_o;    // [batch, hq, max_splits, D]
-  float* part_lse;  // [batch, hq, max_splits] (log2 domain)
+  int32_t max_items;         // kDecodePlanItems + batch: bound of the plan's items
+  int32_t* counter;          // work-item counter (reset by the plan kernel)
+  int32_t* prefix_counter;   // cascade prefix pass's work-item counter (zeroed with the key starts)
+  int32_t* plan;             // [2]: items, keys per item (chunk), written by the plan kernel
+  int32_t* req_item0;        // [batch + 1]: request b's items are req_item0[b] .. req_item0[b+1]-1
+  int32_t* item_req;         // [max_items]: request of each item
+  int32_t* order;            // [max_items]: items in claim order (longest first)
+  float* part_o;    // [max_items, hq, D] per item and q head
+  float* part_lse;  // [max_items, hq] (log2 domain)
   int32_t cchunk;      // shared-prefix keys per prefix-pass split (cascade)
   int32_t max_csplits;  // prefix-pass splits per group range
   int32_t casc_slots;   // prefix partials per (request, q head): levels x max_csplits
@@ -51,16 +53,22 @@ struct DecodeParams {
   uint32_t* err;
 };
 
+// The private keys of a decode call are cut into items on the device (decode_plan_kernel): at most
+// kDecodePlanItems items of equal length (>= kDecodeMinChunk keys) plus one shorter item per request.
+constexpr int32_t kDecodePlanItems = 640;
+constexpr int32_t kDecodeMinChunk = 128;
+
 struct DecodePlan {
-  int32_t chunk = 0;        // private keys per split
-  int32_t max_splits = 0;
+  int32_t max_items = 0;    // kDecodePlanItems + batch
   int32_t cchunk = 0;       // shared-prefix keys per prefix-pass split (cascade)
   int32_t max_csplits = 0;
 };
 
 struct DecodeWorkspace {
   size_t part_o = 0, part_lse = 0, casc_o = 0, casc_lse = 0;
-  size_t ints = 0, ints_bytes = 0;  // one zeroed block: key_start [batch], counter, prefix counter
+  size_t ints = 0, ints_bytes = 0;  // key_start [batch], counter, prefix counter (zeroed with groups);
+                                    // plan [2], req_item0 [batch+1], item_req, order [max_items]
+  size_t zero_bytes = 0;            // leading part of the block cleared before the key-start scatter
   size_t total = 0;
 };
 

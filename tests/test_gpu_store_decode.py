@@ -106,6 +106,20 @@ def test_decode_ragged(seed, hq, hkv, d, max_len):
     check_decode(db)
 
 
+@pytest.mark.parametrize("seed,n,hq,hkv,d,min_len,max_len", [
+    (30, 60, 32, 16, 64, 1, 3000),     # chunk above the minimum, remainders of every size, 2 head groups
+    (31, 5, 8, 2, 128, 256, 256),      # every context an exact multiple of the item length: no short items
+    (32, 3, 8, 2, 64, 127, 129)])      # lengths around one item
+def test_decode_device_plan(seed, n, hq, hkv, d, min_len, max_len):
+    """The call's private keys are cut into items on the device from the real lengths (equal items
+    first, each request's short last item after them): outputs still match the oracle."""
+    b = W.random_mixed(seed, n_extend=0, n_decode=n, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                       min_len=min_len, max_len=max_len)
+    db = DeviceBatch(b)
+    db.store()
+    check_decode(db)
+
+
 def test_decode_single_token_contexts():
     b = W.random_mixed(8, n_extend=0, n_decode=5, num_q_heads=8, num_kv_heads=2, head_dim=128, max_len=1,
                        min_len=1, share_prob=0.0)

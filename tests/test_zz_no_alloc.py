@@ -77,8 +77,8 @@ def test_static_scratch_decode_matches_workspace_decode_on_two_calls():
 
 
 def test_static_scratch_decode_rejects_sizes_beyond_the_array():
-    # 224 requests x 64 q heads with contexts up to 32K need far more than 32 MiB of partials
-    need = ra.ra_decode_workspace_bytes(224, 64, 8, 128, 32768)
+    # 4096 requests x 64 q heads need more than 32 MiB of partials
+    need = ra.ra_decode_workspace_bytes(4096, 64, 8, 128, 32768)
     assert need > ra.RA_DECODE_STATIC_SCRATCH_BYTES
     b = W.random_mixed(32, n_extend=0, n_decode=2, num_q_heads=64, num_kv_heads=8, head_dim=128, max_len=50)
     db = DeviceBatch(b)
@@ -88,7 +88,7 @@ def test_static_scratch_decode_rejects_sizes_beyond_the_array():
     st = lib.ra_decode_attention_static(
         P(db.k_pool.data_ptr()), P(db.v_pool.data_ptr()), b.num_slots, 8, 128, P(db.dec_q.data_ptr()),
         P(out.data_ptr()), 64, b.sm_scale, P(db.table.data_ptr()), 32768, db.table.shape[0],
-        P(db.dec_rpi.data_ptr()), P(db.dec_lens.data_ptr()), 224, 32768, 0, None, None, None, None, None, 0, 0, 1,
+        P(db.dec_rpi.data_ptr()), P(db.dec_lens.data_ptr()), 4096, 32768, 0, None, None, None, None, None, 0, 0, 1,
         None, P(torch.cuda.current_stream(db.dev).cuda_stream))
     assert st == 3  # RA_ERR_WORKSPACE, nothing launched
     assert b"static scratch" in lib.ra_last_error_message()
