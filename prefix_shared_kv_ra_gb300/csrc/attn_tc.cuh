@@ -137,6 +137,8 @@ struct Job {
   int32_t mem0;      // cascade: first member index into group_reqs
   int32_t csplit;    // cascade: prefix split
   int32_t slot;      // cascade: partial slot of the members (level x max_csplits + split)
+  int32_t tiles;     // query tiles holding valid rows (1: tile 1 is empty; its MMAs and softmax are skipped,
+                     // while every barrier still completes its phases as for two tiles)
 };
 
 // Item -> job; false for an empty or invalid item (reported once, when `report`).
@@ -201,6 +203,7 @@ __device__ __forceinline__ bool tc_job(const TcParams& p, int32_t item, Job& j, 
     }
   }
   j.nt = (j.kend - j.kbeg + kKeys - 1) / kKeys;
+  j.tiles = j.n_valid > T ? 2 : 1;
   return j.nt > 0;
 }
 
@@ -471,7 +474,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       load_q(jb, 0);
       load_q(jb, 1);
     }
-    auto qk = [&](int i, int gg) -> bool {  // S_i = Q_i K_gg^T
+    // S_i = Q_i K_gg^T; for an empty query tile (live false) only the commit, which keeps bar_s's phases
+    auto qk = [&](int i, int gg, bool live) -> bool {
       const int st = gg % KS;
       if (i == 0) {
         if (!wait_all(bar_kf[st], (gg / KS) & 1)) return false;
@@ -479,7 +483,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       }
       if (lane == 0) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D / 16 && live; ++kk) {
           const uint32_t off = (kk >> 2) * (kRows * 128) + (kk & 3) * 32;
           tc_mma_ss(tmem + i * kKeys, sdesc_sw128(sQ(i) + off, 16, 1024), sdesc_sw128(sK(st) + off, 16, 1024),
                     idesc_qk, kk > 0);
@@ -505,8 +509,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         tc_fence_after();
       }
       if (lane == 0) {
+        const bool live = i < jb.tiles;  // an empty query tile issues no PV (its O is never read)
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
+        for (int kk = 0; kk < kKeys / 16 && live; ++kk) {
           tc_mma_ts(tmem + kColO + i * 128, tmem + i * kKeys + kk * 8,
                     sdesc_sw128(sV(st) + kk * 2048, kRows * 128, 1024), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         }
@@ -534,13 +539,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     auto qk_first = [&](int i, int gg) -> bool {  // item n+1's first QK on tile i
       if (!wait_all(bar_q[i], (n + 1) & 1)) return false;
       tc_fence_after();
-      return qk(i, gg);
+      return qk(i, gg, i < jn.tiles);
     };
     if (ok && r > 0) {
       ok = wait_all(bar_q[0], 0) && wait_all(bar_q[1], 0);
       if (ok) {
         tc_fence_after();
-        ok = qk(0, 0) && qk(1, 0);
+        ok = qk(0, 0, true) && qk(1, 0, jb.tiles > 1);
       }
     }
     while (ok && r > 0) {
@@ -548,7 +553,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         if (aborted(abort_flag)) { ok = false; break; }
         const int gg = g + j;
         if (j + 1 < jb.nt) {
-          ok = pv(0, gg, j) && qk(0, gg + 1) && pv(1, gg, j) && qk(1, gg + 1);
+          ok = pv(0, gg, j) && qk(0, gg + 1, true) && pv(1, gg, j) && qk(1, gg + 1, jb.tiles > 1);
         } else {
           ok = reload_q(0, gg) && pv(0, gg, j) && reload_q(1, gg) && (next == 0 || qk_first(0, gg + 1)) &&
                pv(1, gg, j) && (next == 0 || qk_first(1, gg + 1));
@@ -590,6 +595,10 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         const int gg = g + j;
         const bool fail_here = aborted(abort_flag) || !mbar_wait(smem_u32(&bar_s[ti]), gg & 1);
         if (__any_sync(0xffffffffu, fail_here)) { ok = false; break; }  // warp-uniform: tcgen05.ld/st are collective
+        if (ti >= jb.tiles) {  // an empty query tile: no S was computed; keep bar_p's phase
+          mbar_arrive(smem_u32(&bar_p[ti]));
+          continue;
+        }
         tc_fence_after();
         const int32_t key0 = jb.kbeg + j * kKeys;
         const bool masked = key0 + kKeys > lim;
