@@ -55,7 +55,10 @@ struct DecodeParams {
 
 // The private keys of a decode call are cut into items on the device (decode_plan_kernel): at most
 // kDecodePlanItems items of equal length (>= kDecodeMinChunk keys) plus one shorter item per request.
-constexpr int32_t kDecodePlanItems = 640;
+// Three full-length items per SM of GB300 (152 SMs): measured against 320 and 640, the best or tied on
+// the decode workloads (forked 70B 185 / 244 / 210 us, multi-turn mix 266 / 265 / 278 us).  A constant,
+// not the device's SM count: the workspace size must not depend on the device that runs the call.
+constexpr int32_t kDecodePlanItems = 456;
 constexpr int32_t kDecodeMinChunk = 128;
 
 struct DecodePlan {
