@@ -386,14 +386,15 @@ __global__ void __launch_bounds__(32 * kCombineWarps) decode_combine_kernel(cons
   const int lane = threadIdx.x & 31;
   if (warp_global >= p.batch * p.hq) return;
   const int b = warp_global / p.hq;
+  // the request's description, loaded together (one round trip)
   int32_t L = __ldg(p.seq_lens + b);
   const int32_t row = __ldg(p.rpi + b);
-  if (row < 0 || row >= p.table_rows || L < 1) return;
-  if (L > p.max_seq_len) L = p.max_seq_len;
   int32_t start = p.key_start ? __ldg(p.key_start + b) : 0;
-  start = start < 0 ? 0 : (start > L ? L : start);
   const int32_t i0 = p.req_item0[b];  // the request's private items are i0 .. i0 + n_splits - 1
   const int32_t n_splits = p.req_item0[b + 1] - i0;
+  if (row < 0 || row >= p.table_rows || L < 1) return;
+  if (L > p.max_seq_len) L = p.max_seq_len;
+  start = start < 0 ? 0 : (start > L ? L : start);
   // prefix partials: every slot of every level; those no group wrote hold -inf (weight 0, skipped)
   const int32_t n_pre = start > 0 ? p.casc_slots : 0;
   if (n_splits == 1 && n_pre == 0) return;  // written directly by the decode kernel

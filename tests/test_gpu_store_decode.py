@@ -120,6 +120,17 @@ def test_decode_device_plan(seed, n, hq, hkv, d, min_len, max_len):
     check_decode(db)
 
 
+def test_decode_device_plan_large_batch():
+    """More requests than the plan kernel has threads (each thread plans a run of consecutive requests),
+    short contexts; without and with cascade groups."""
+    b = W.random_mixed(33, n_extend=0, n_decode=2500, num_q_heads=8, num_kv_heads=2, head_dim=64, max_len=40,
+                       with_cascade=True)
+    db = DeviceBatch(b)
+    db.store()
+    check_decode(db)
+    check_decode(db, cascade=True)
+
+
 def test_decode_single_token_contexts():
     b = W.random_mixed(8, n_extend=0, n_decode=5, num_q_heads=8, num_kv_heads=2, head_dim=128, max_len=1,
                        min_len=1, share_prob=0.0)
