@@ -602,30 +602,34 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         tc_fence_after();
         const int32_t key0 = jb.kbeg + j * kKeys;
         const bool masked = key0 + kKeys > lim;
-        // Tiles after the first are exponentiated against the current reference in a single pass.  The
-        // row sum bounds every probability of the row (p <= sum), so a sum above kFastSumLimit, or one
-        // that is not finite, marks the reference as stale: the warp then redoes the tile on the exact
-        // path -- row maximum first, lazy reference update, then the exponentials -- which the first
-        // tile always takes.  P is held in registers until the pass is accepted, since it overwrites S.
+        // Every tile is exponentiated against a reference in a single pass: the current one, or on the
+        // item's first tile the maximum of its first 32 columns.  The row sum bounds every probability
+        // of the row (p <= sum), so a sum above kFastSumLimit, or one that is not finite, marks the
+        // reference as stale: the warp then redoes the tile on the exact path -- row maximum first, lazy
+        // reference update, then the exponentials.  P is held in registers until the pass is accepted,
+        // since it overwrites S.
         uint32_t pk[2][32];
         float rowsum = 0.f, alpha = 1.f, m_ref = m_used;
         bool resc = false;
-        bool exact = j == 0;
+        bool exact = false;
 #pragma unroll 1
         for (int attempt = 0; attempt < 2; ++attempt) {
+          // row max of the raw scores (scale > 0 commutes with max), 8 independent chains
+          float mx8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+          auto max_chunk = [&](const uint32_t (&sr)[32], int c) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float x = (masked && key0 + c * 32 + e >= lim) ? -INFINITY : __uint_as_float(sr[e]);
+              mx8[e & 7] = fmaxf(mx8[e & 7], x);
+            }
+          };
+          auto max_of = [&]() {
+            return fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.scale_log2;
+          };
           if (exact) {
-            // row max of the raw scores (scale > 0 commutes with max), 8 independent chains; the next
-            // 32-column TMEM load is in flight while the current chunk is reduced
-            float mx8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-            auto max_chunk = [&](const uint32_t (&sr)[32], int c) {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const float x = (masked && key0 + c * 32 + e >= lim) ? -INFINITY : __uint_as_float(sr[e]);
-                mx8[e & 7] = fmaxf(mx8[e & 7], x);
-              }
-            };
             uint32_t ba[32], bb[32];
             tmem_ld32(tmem + lane_addr + col_s, ba);
             tc_wait_ld_regs(ba);
@@ -639,11 +643,17 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
             max_chunk(ba, 2);
             tc_wait_ld_regs(bb);
             max_chunk(bb, 3);
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * p.scale_log2;
-            const float m_new = fmaxf(m_used, mx);
+            const float m_new = fmaxf(m_used, max_of());
             resc = m_new > m_used + kRescaleThreshold;
             m_ref = resc ? m_new : m_used;
+          } else if (j == 0) {
+            // the item's first tile: the reference is the maximum of chunk 0 (it holds a key of every
+            // row: the row's first key is the tile's first).  O and l are empty, nothing to rescale.
+            uint32_t ba[32];
+            tmem_ld32(tmem + lane_addr + col_s, ba);
+            tc_wait_ld_regs(ba);
+            max_chunk(ba, 0);
+            m_ref = max_of();
           }
           const float m_sub = (m_ref == -INFINITY) ? 0.f : m_ref;
           alpha = resc ? ex2(m_used - m_sub) : 1.f;
