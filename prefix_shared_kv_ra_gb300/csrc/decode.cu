@@ -506,15 +506,14 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
   __shared__ int32_t s_wa[32], s_wb[32];
   __shared__ int32_t s_hist[kRemBuckets];
   __shared__ unsigned long long s_total;
-  // Without groups this is the call's first kernel: it waits for earlier kernels (they may still use the
-  // workspace) and lets the decode kernel launch at once (the decode kernel waits for this grid before its
-  // first claim).  With groups it runs behind the prefix pass, which let it launch only after the key
-  // starts were complete; it does not wait for the pass, so that the decode kernel can run beside it.
+  // Without groups this is the call's first kernel: it lets the decode kernel launch at once (the decode
+  // kernel waits for this grid before its first claim) and plans from the call's inputs, which no kernel
+  // of this library writes, while the kernel before it finishes; it waits for that kernel only before its
+  // first write to the workspace (the kernel may be the previous call's combine, still reading it).
+  // With groups it runs behind the prefix pass, which let it launch only after the key starts were
+  // complete; it does not wait for the pass, so that the decode kernel can run beside it.
   const bool behind_pass = p.key_start != nullptr;
-  if (!behind_pass) {
-    griddep_wait();
-    griddep_launch();
-  }
+  if (!behind_pass) griddep_launch();
   const int t = threadIdx.x;
   const int32_t per = (p.batch + kPlanThreads - 1) / kPlanThreads;
   const int32_t r0 = min(p.batch, t * per), r1 = min(p.batch, r0 + per);
@@ -566,6 +565,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
     }
   }
   __syncthreads();
+  if (!behind_pass) griddep_wait();  // the workspace is free
   for (int32_t b = r0; b < r1; ++b) {
     const int32_t len = len_of(b, false);
     const int32_t c = (len + chunk - 1) / chunk, f = len / chunk, rem = len % chunk;

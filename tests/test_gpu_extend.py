@@ -43,6 +43,19 @@ def test_extend_ragged(seed, hq, hkv, d, max_len):
     check_extend(db)
 
 
+@pytest.mark.parametrize("d", [128, 64])
+def test_extend_output_only_16_byte_aligned(d):
+    """An output only as aligned as the interface requires (16 bytes: a view 16 bytes into a buffer)."""
+    b = W.random_mixed(40 + d, n_extend=5, n_decode=0, num_q_heads=16, num_kv_heads=4, head_dim=d, max_len=400)
+    db = DeviceBatch(b)
+    db.store()
+    n = db.ext_o.numel()
+    big = torch.full((n + 8,), float("nan"), dtype=torch.bfloat16, device=db.dev)
+    db.ext_o = big[8:].view(db.ext_o.shape)
+    assert db.ext_o.data_ptr() % 32 == 16
+    check_extend(db)
+
+
 def test_extend_prefix_zero_and_single_token_suffix():
     b = W.random_mixed(11, n_extend=5, n_decode=0, num_q_heads=32, num_kv_heads=8, head_dim=128, max_len=300,
                        share_prob=0.0, ext_lens=[1, 300, 1, 129, 128])
