@@ -183,11 +183,13 @@ def with_tree_groups(b, min_prefix: int = 256, multilevel: bool = False):
 class Step:
     """The hot path on one batch, resident on the device."""
 
-    def __init__(self, b, dev, cascade: bool = False):
+    def __init__(self, b, dev, cascade: bool = False, fused_store: bool = False):
         import torch
         import prefix_shared_kv_ra_gb300 as ra
         self.torch, self.ra, self.b, self.dev = torch, ra, b, dev
         self.cascade = cascade and b.has_cascade()
+        # decode-only batch: the store of its new tokens fused into the decode call (one launch fewer)
+        self.fused_store = fused_store and b.n_extend == 0 and b.n_decode > 0
 
         def bf16(a):
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -229,6 +231,8 @@ class Step:
         # kernel launches per step: store, [work-list plan, extend,] [[zeroing, key_start scatter,] decode
         # plan, [prefix pass,] decode, combine]
         self.launches = 1 + (2 if b.n_extend else 0) + ((3 + (3 if self.cascade else 0)) if b.n_decode else 0)
+        if self.fused_store:
+            self.launches -= 1
 
     def run(self, d=None, events=None, outs=None):
         ra, b = self.ra, self.b
@@ -237,6 +241,14 @@ class Step:
         ev = events or [None] * 4
         if ev[0] is not None:
             ev[0].record()
+        if self.fused_store:
+            ra.ra_decode_attention_store(self.k_pool, self.v_pool, d["k_new"], d["v_new"], d["loc"], d["dec_q"],
+                                         dec_o, self.table, d["dec_rpi"], d["dec_lens"], max_seq_len=b.max_seq_len,
+                                         sm_scale=b.sm_scale, workspace=self.ws, device_error=self.err, **self.casc)
+            for e in ev[1:]:
+                if e is not None:
+                    e.record()
+            return
         ra.ra_kv_store(self.k_pool, self.v_pool, d["k_new"], d["v_new"], d["loc"], device_error=self.err)
         if ev[1] is not None:
             ev[1].record()
@@ -383,6 +395,24 @@ def extra_kernels(dev, flush, peaks, reps: int = 20):
                             "effective_gbs": db["logical"] / ms / 1e6}
             out[key]["device_error"] = r["device_error"]
             del st
+    # the decode step's store fused into the decode call, against the two calls (whole steps, no events
+    # between the calls, so the programmatic launch chain is kept in both)
+    b = W.cfg2_decode_8b()
+    steps = {}
+    for fused in (False, True):
+        st = Step(b, dev, fused_store=fused)
+        st.run()
+        r = time_steps(st, reps, 3, flush, breakdown=False)
+        steps[fused] = (float(np.median(r["step_ms"])), r["device_error"])
+        del st
+    nbytes = decode_bytes(b)["algorithmic"] + store_bytes(b)
+    ms = steps[True][0]
+    out["decode_8b_system_prompts_store_fused"] = {
+        "kernel": "store + decode in one call (ra_decode_attention_store)", "ms": ms,
+        "separate_store_then_decode_ms": steps[False][0], "tokens_per_s": b.n_decode / ms * 1e3,
+        "algorithmic_bytes": nbytes, "gbs": nbytes / ms / 1e6,
+        "frac_of_measured_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"],
+        "device_error": steps[True][1] | steps[False][1]}
     return out
 
 

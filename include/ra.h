@@ -187,6 +187,37 @@ size_t ra_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num
                                  int32_t max_group_size, int32_t max_group_levels);
 
 /*
+ * ra_decode_attention_store -- ra_kv_store of the decode step's new tokens and
+ * ra_decode_attention in one call, the store fused into the call's first
+ * kernel (one launch fewer per step).  A decode step writes one new token per
+ * request at out_cache_loc and then attends over the context that includes it
+ * (anrans handbook "v0.2：不到四千行的调度核心跑出 3.1 倍", 来源一: the decode
+ * inputs req_pool_indices, seq_lens and out_cache_loc).
+ *   k_new, v_new: bf16 [batch, num_kv_heads, head_dim], row b = request b's
+ *     new token; out_cache_loc: int32 [batch], its slot.  The pool is written
+ *     as by ra_kv_store(k_pool, v_pool, ..., k_new, v_new, out_cache_loc,
+ *     batch, ...) (bit copy; a slot outside the pool is skipped and flagged
+ *     RA_DEVERR_SLOT), before any key is read; the caller has already listed
+ *     out_cache_loc[b] in req_to_token at position seq_lens[b] - 1 (or wherever
+ *     its table says), exactly as for ra_kv_store followed by
+ *     ra_decode_attention.
+ *   Every other argument, the workspace size and the result are those of
+ *   ra_decode_attention.  k_new / v_new 16-byte aligned, out_cache_loc 4-byte
+ *   aligned; all three non-null.
+ */
+ra_status ra_decode_attention_store(void* k_pool, void* v_pool, int64_t num_slots, int32_t num_kv_heads,
+                                    int32_t head_dim, const void* k_new, const void* v_new,
+                                    const int32_t* out_cache_loc, const void* q, void* o, int32_t num_q_heads,
+                                    float sm_scale, const int32_t* req_to_token, int64_t table_stride,
+                                    int64_t table_rows, const int32_t* req_pool_indices, const int32_t* seq_lens,
+                                    int32_t batch, int32_t max_seq_len, int32_t num_groups,
+                                    const int32_t* group_indptr, const int32_t* group_reqs,
+                                    const int32_t* group_prefix_start, const int32_t* group_prefix_len,
+                                    const int32_t* group_level, int32_t max_group_prefix_len, int32_t max_group_size,
+                                    int32_t max_group_levels, void* workspace, size_t workspace_bytes,
+                                    uint32_t* device_error, ra_stream_t stream);
+
+/*
  * ra_decode_attention_static -- ra_decode_attention for callers that cannot
  * allocate device memory.  The paper has no counterpart: this is an interface
  * addition for callers such as a plugin that runs under a host framework's
@@ -224,7 +255,7 @@ const char* ra_last_error_message(void);
 /* ABI revision of this header (bumped on any signature change). */
 int32_t ra_abi_version(void);
 
-#define RA_ABI_VERSION 3
+#define RA_ABI_VERSION 4
 
 #ifdef __cplusplus
 }

@@ -23,7 +23,7 @@ import torch
 from . import _build
 
 __all__ = ["RAError", "ra_kv_store", "ra_extend_attention", "ra_extend_workspace_bytes", "ra_decode_attention",
-           "ra_decode_workspace_bytes",
+           "ra_decode_workspace_bytes", "ra_decode_attention_store",
            "ra_decode_attention_static", "RA_DECODE_STATIC_SCRATCH_BYTES",
            "ra_abi_version", "library_path", "load", "DEVERR_SLOT", "DEVERR_TABLE", "DEVERR_LENGTH",
            "DEVERR_TIMEOUT"]
@@ -62,6 +62,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.ra_extend_workspace_bytes.restype = sz
     lib.ra_decode_attention.argtypes = [P, P, i64, i32, i32, P, P, i32, f32, P, i64, i64, P, P, i32, i32, i32,
                                         P, P, P, P, P, i32, i32, i32, P, sz, P, P]
+    lib.ra_decode_attention_store.argtypes = [P, P, i64, i32, i32, P, P, P, P, P, i32, f32, P, i64, i64, P, P, i32,
+                                              i32, i32, P, P, P, P, P, i32, i32, i32, P, sz, P, P]
+    lib.ra_decode_attention_store.restype = ctypes.c_int
     lib.ra_decode_attention_static.argtypes = [P, P, i64, i32, i32, P, P, i32, f32, P, i64, i64, P, P, i32, i32,
                                                i32, P, P, P, P, P, i32, i32, i32, P, P]
     lib.ra_decode_attention_static.restype = ctypes.c_int
@@ -178,6 +181,41 @@ def ra_decode_attention(k_pool: torch.Tensor, v_pool: torch.Tensor, q: torch.Ten
         raise ValueError("workspace must be a contiguous uint8 tensor on the pool's device")
     _check(load().ra_decode_attention(
         _ptr(k_pool, bf, "k_pool", dev), _ptr(v_pool, bf, "v_pool", dev), S, hkv, d, _ptr(q, bf, "q", dev),
+        _ptr(o, bf, "o", dev), hq, float(sm_scale), _ptr(req_to_token, i32, "req_to_token", dev),
+        req_to_token.shape[1], req_to_token.shape[0], _ptr(req_pool_indices, i32, "req_pool_indices", dev),
+        _ptr(seq_lens, i32, "seq_lens", dev), batch, int(max_seq_len), ng,
+        _ptr(group_indptr, i32, "group_indptr", dev), _ptr(group_reqs, i32, "group_reqs", dev),
+        _ptr(group_prefix_start, i32, "group_prefix_start", dev), _ptr(group_prefix_len, i32, "group_prefix_len", dev),
+        _ptr(group_level, i32, "group_level", dev), int(max_group_prefix_len), int(max_group_size),
+        int(max_group_levels), ctypes.c_void_p(workspace.data_ptr()), workspace.numel(),
+        _ptr(device_error, i32, "device_error", dev), _stream(dev, stream)))
+
+
+def ra_decode_attention_store(k_pool: torch.Tensor, v_pool: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                              out_cache_loc: torch.Tensor, q: torch.Tensor, o: torch.Tensor,
+                              req_to_token: torch.Tensor, req_pool_indices: torch.Tensor, seq_lens: torch.Tensor, *,
+                              max_seq_len: int, sm_scale: float, workspace: torch.Tensor,
+                              group_indptr: Optional[torch.Tensor] = None, group_reqs: Optional[torch.Tensor] = None,
+                              group_prefix_len: Optional[torch.Tensor] = None, max_group_prefix_len: int = 0,
+                              max_group_size: int = 0, group_prefix_start: Optional[torch.Tensor] = None,
+                              group_level: Optional[torch.Tensor] = None, max_group_levels: int = 1,
+                              device_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """The decode step's store and attention in one call: pool[out_cache_loc[b]] = k_new[b] / v_new[b]
+    ([batch, Hkv, D] bf16), then ra_decode_attention (same arguments and result)."""
+    dev = k_pool.device
+    S, hkv, d = k_pool.shape
+    batch, hq, dq = q.shape
+    if dq != d or o.shape != q.shape:
+        raise ValueError("q/o shape mismatch")
+    if k_new.shape != (batch, hkv, d) or v_new.shape != k_new.shape or out_cache_loc.shape != (batch,):
+        raise ValueError("k_new / v_new must be [batch, Hkv, D] and out_cache_loc [batch]")
+    bf, i32 = torch.bfloat16, torch.int32
+    ng = 0 if group_indptr is None else group_indptr.shape[0] - 1
+    if workspace.dtype != torch.uint8 or not workspace.is_contiguous() or workspace.device != dev:
+        raise ValueError("workspace must be a contiguous uint8 tensor on the pool's device")
+    _check(load().ra_decode_attention_store(
+        _ptr(k_pool, bf, "k_pool", dev), _ptr(v_pool, bf, "v_pool", dev), S, hkv, d, _ptr(k_new, bf, "k_new", dev),
+        _ptr(v_new, bf, "v_new", dev), _ptr(out_cache_loc, i32, "out_cache_loc", dev), _ptr(q, bf, "q", dev),
         _ptr(o, bf, "o", dev), hq, float(sm_scale), _ptr(req_to_token, i32, "req_to_token", dev),
         req_to_token.shape[1], req_to_token.shape[0], _ptr(req_pool_indices, i32, "req_pool_indices", dev),
         _ptr(seq_lens, i32, "seq_lens", dev), batch, int(max_seq_len), ng,

@@ -502,7 +502,35 @@ __device__ __forceinline__ void plan_scan2(int32_t& a, int32_t& b, int32_t& ta, 
 // item first, then each request's shorter last item by decreasing size (longest processing time first),
 // so the CTAs that finish last finish on short items.  One CTA of kPlanThreads threads; each thread owns
 // a contiguous run of requests.  It also resets the work counter.
+// Fused store (ra_decode_attention_store): pool[st_loc[b]] = new row b for K and V, one 16-byte vector
+// per thread and step, consecutive threads on consecutive vectors of a row (as ra_kv_store).  Run by
+// the call's first kernel after it waited for the kernels before it (they may still read the slots).
+__device__ __forceinline__ void scatter_new_rows(const DecodeParams& p, int64_t first, int64_t stride) {
+  uint4* kp = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(p.k_pool));
+  uint4* vp = reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(p.v_pool));
+  for (int64_t i = first; i < p.st_total; i += stride) {
+    const int64_t b = i / p.st_row_vecs;
+    const int32_t c = static_cast<int32_t>(i - b * p.st_row_vecs);
+    const int32_t slot = __ldg(p.st_loc + b);
+    if (slot < 0 || slot >= p.num_slots) {
+      if (c == 0) flag_error(p.err, RA_DEVERR_SLOT);
+      continue;
+    }
+    const uint4 kv = __ldg(p.st_k + i), vv = __ldg(p.st_v + i);
+    const int64_t dst = static_cast<int64_t>(slot) * p.st_row_vecs + c;
+    kp[dst] = kv;
+    vp[dst] = vv;
+  }
+}
+
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeParams p) {
+  if (blockIdx.x > 0) {  // the fused store's CTAs (only without groups; CTA 0 plans)
+    griddep_launch();
+    griddep_wait();
+    scatter_new_rows(p, static_cast<int64_t>(blockIdx.x - 1) * blockDim.x + threadIdx.x,
+                     static_cast<int64_t>(gridDim.x - 1) * blockDim.x);
+    return;
+  }
   __shared__ int32_t s_wa[32], s_wb[32];
   __shared__ int32_t s_hist[kRemBuckets];
   __shared__ unsigned long long s_total;
@@ -593,11 +621,17 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
   }
 }
 
-// Zero the workspace's integer block (work counters, key starts) at the head of the call.
-__global__ void zero_ints_kernel(int32_t* x, int32_t n) {
-  griddep_wait();  // earlier kernels on the stream may still use the workspace
+// Zero the workspace's integer block (work counters, key starts) at the head of a call with cascade
+// groups; with a fused store, CTAs 1.. scatter the step's new rows.
+__global__ void zero_ints_kernel(const DecodeParams p, int32_t* x, int32_t n) {
+  griddep_wait();  // earlier kernels on the stream may still use the workspace and the pool
   griddep_launch();
-  for (int32_t i = threadIdx.x; i < n; i += blockDim.x) x[i] = 0;
+  if (blockIdx.x == 0) {
+    for (int32_t i = threadIdx.x; i < n; i += blockDim.x) x[i] = 0;
+  } else {
+    scatter_new_rows(p, static_cast<int64_t>(blockIdx.x - 1) * blockDim.x + threadIdx.x,
+                     static_cast<int64_t>(gridDim.x - 1) * blockDim.x);
+  }
 }
 
 // key_start[b] = the largest range end of b's cascade groups (0 for requests in no group, set by the
@@ -736,19 +770,19 @@ extern "C" size_t ra_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, 
       .total;
 }
 
-extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool, int64_t num_slots,
-                                         int32_t num_kv_heads, int32_t head_dim, const void* q, void* o,
-                                         int32_t num_q_heads, float sm_scale, const int32_t* req_to_token,
-                                         int64_t table_stride, int64_t table_rows, const int32_t* req_pool_indices,
-                                         const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
-                                         int32_t num_groups, const int32_t* group_indptr,
-                                         const int32_t* group_reqs, const int32_t* group_prefix_start,
-                                         const int32_t* group_prefix_len, const int32_t* group_level,
-                                         int32_t max_group_prefix_len, int32_t max_group_size,
-                                         int32_t max_group_levels, void* workspace, size_t workspace_bytes,
-                                         uint32_t* device_error, ra_stream_t stream) {
+// ra_decode_attention, and with k_new / v_new / out_cache_loc non-null ra_decode_attention_store.
+static ra_status decode_call(const void* k_pool, const void* v_pool, int64_t num_slots, int32_t num_kv_heads,
+                             int32_t head_dim, const void* k_new, const void* v_new, const int32_t* out_cache_loc,
+                             const void* q, void* o, int32_t num_q_heads, float sm_scale,
+                             const int32_t* req_to_token, int64_t table_stride, int64_t table_rows,
+                             const int32_t* req_pool_indices, const int32_t* seq_lens, int32_t batch,
+                             int32_t max_seq_len, int32_t num_groups, const int32_t* group_indptr,
+                             const int32_t* group_reqs, const int32_t* group_prefix_start,
+                             const int32_t* group_prefix_len, const int32_t* group_level,
+                             int32_t max_group_prefix_len, int32_t max_group_size, int32_t max_group_levels,
+                             void* workspace, size_t workspace_bytes, uint32_t* device_error, ra_stream_t stream) {
   using namespace ra;
-  clear_error();
+  const bool fused = k_new != nullptr || v_new != nullptr || out_cache_loc != nullptr;
   RA_REQUIRE(batch >= 0 && batch <= 65535, "batch must be in [0, 65535] (got %d)", batch);
   RA_REQUIRE(num_kv_heads > 0 && num_q_heads > 0, "head counts must be > 0");
   RA_REQUIRE(num_q_heads % num_kv_heads == 0, "num_q_heads (%d) must be a multiple of num_kv_heads (%d)",
@@ -769,6 +803,11 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
              "pools, q and o must be 16-byte aligned");
   RA_REQUIRE(aligned4(req_to_token) && aligned4(req_pool_indices) && aligned4(seq_lens),
              "index arrays must be 4-byte aligned");
+  if (fused) {
+    RA_REQUIRE(k_new && v_new && out_cache_loc, "k_new, v_new and out_cache_loc must all be non-null");
+    RA_REQUIRE(aligned16(k_new) && aligned16(v_new) && aligned4(out_cache_loc),
+               "k_new and v_new must be 16-byte aligned, out_cache_loc 4-byte aligned");
+  }
   if (num_groups > 0) {
     RA_REQUIRE(group_indptr && group_reqs && group_prefix_len, "cascade arrays must be non-null");
     RA_REQUIRE(max_group_prefix_len >= 1 && max_group_prefix_len <= max_seq_len,
@@ -814,6 +853,22 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
   p.part_lse = reinterpret_cast<float*>(ws + wl.part_lse);
   p.err = device_error;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // fused store: extra CTAs of the call's first kernel scatter the new rows (a few waves of 4 vectors
+  // per thread, at most one CTA per SM)
+  int store_ctas = 0;
+  if (fused) {
+    DeviceInfo d0;
+    if (ra_status st = current_device(&d0)) return st;
+    p.st_k = static_cast<const uint4*>(k_new);
+    p.st_v = static_cast<const uint4*>(v_new);
+    p.st_loc = out_cache_loc;
+    p.st_row_vecs = num_kv_heads * head_dim * 2 / 16;
+    p.st_total = static_cast<int64_t>(batch) * p.st_row_vecs;
+    const int64_t per_cta = (num_groups > 0 ? 256 : kPlanThreads) * 4;
+    const int64_t want = (p.st_total + per_cta - 1) / per_cta;
+    store_ctas = static_cast<int>(want < d0.num_sms ? want : d0.num_sms);
+    if (store_ctas < 1) store_ctas = 1;
+  }
 
   int32_t* ints = reinterpret_cast<int32_t*>(ws + wl.ints);
   p.counter = ints + batch;
@@ -832,8 +887,8 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
     p.casc_o = reinterpret_cast<float*>(ws + wl.casc_o);
     p.casc_lse = reinterpret_cast<float*>(ws + wl.casc_lse);
     p.key_start = ints;
-    if (ra_status st = launch_pdl("zero_ints_kernel", zero_ints_kernel, dim3(1), dim3(256), 0, s, ints,
-                                  static_cast<int32_t>(wl.zero_bytes / sizeof(int32_t))))
+    if (ra_status st = launch_pdl("zero_ints_kernel", zero_ints_kernel, dim3(1 + store_ctas), dim3(256), 0, s, p,
+                                  ints, static_cast<int32_t>(wl.zero_bytes / sizeof(int32_t))))
       return st;
     if (ra_status st = launch_pdl("cascade_key_start_kernel", cascade_key_start_kernel, dim3((batch + 127) / 128),
                                   dim3(128), 0, s, ints, batch, group_indptr, group_reqs, group_prefix_len, num_groups,
@@ -845,7 +900,9 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
                    num_groups,           max_group_prefix_len, max_group_size,     max_group_levels};
     if (ra_status st = launch_cascade_prefix(p, ca, head_dim, s)) return st;
   }
-  if (ra_status st = launch_pdl("decode_plan_kernel", decode_plan_kernel, dim3(1), dim3(kPlanThreads), 0, s, p))
+  // (with groups the zeroing kernel did the fused store: the plan kernel runs behind the prefix pass)
+  if (ra_status st = launch_pdl("decode_plan_kernel", decode_plan_kernel, dim3(1 + (num_groups > 0 ? 0 : store_ctas)),
+                                dim3(kPlanThreads), 0, s, p))
     return st;
   // persistent decode geometry
   p.hpc = heads_per_cta(num_kv_heads);
@@ -861,4 +918,45 @@ extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool,
   if (ra_status st = current_device(&dev)) return st;
   const int grid = static_cast<int>(n_items < dev.num_sms ? n_items : dev.num_sms);
   return head_dim == 128 ? launch_decode<128>(p, grid, smem, s) : launch_decode<64>(p, grid, smem, s);
+}
+
+extern "C" ra_status ra_decode_attention(const void* k_pool, const void* v_pool, int64_t num_slots,
+                                         int32_t num_kv_heads, int32_t head_dim, const void* q, void* o,
+                                         int32_t num_q_heads, float sm_scale, const int32_t* req_to_token,
+                                         int64_t table_stride, int64_t table_rows, const int32_t* req_pool_indices,
+                                         const int32_t* seq_lens, int32_t batch, int32_t max_seq_len,
+                                         int32_t num_groups, const int32_t* group_indptr,
+                                         const int32_t* group_reqs, const int32_t* group_prefix_start,
+                                         const int32_t* group_prefix_len, const int32_t* group_level,
+                                         int32_t max_group_prefix_len, int32_t max_group_size,
+                                         int32_t max_group_levels, void* workspace, size_t workspace_bytes,
+                                         uint32_t* device_error, ra_stream_t stream) {
+  ra::clear_error();
+  return decode_call(k_pool, v_pool, num_slots, num_kv_heads, head_dim, nullptr, nullptr, nullptr, q, o,
+                     num_q_heads, sm_scale, req_to_token, table_stride, table_rows, req_pool_indices, seq_lens, batch,
+                     max_seq_len, num_groups, group_indptr, group_reqs, group_prefix_start, group_prefix_len,
+                     group_level, max_group_prefix_len, max_group_size, max_group_levels, workspace, workspace_bytes,
+                     device_error, stream);
+}
+
+extern "C" ra_status ra_decode_attention_store(void* k_pool, void* v_pool, int64_t num_slots, int32_t num_kv_heads,
+                                               int32_t head_dim, const void* k_new, const void* v_new,
+                                               const int32_t* out_cache_loc, const void* q, void* o,
+                                               int32_t num_q_heads, float sm_scale, const int32_t* req_to_token,
+                                               int64_t table_stride, int64_t table_rows,
+                                               const int32_t* req_pool_indices, const int32_t* seq_lens,
+                                               int32_t batch, int32_t max_seq_len, int32_t num_groups,
+                                               const int32_t* group_indptr, const int32_t* group_reqs,
+                                               const int32_t* group_prefix_start, const int32_t* group_prefix_len,
+                                               const int32_t* group_level, int32_t max_group_prefix_len,
+                                               int32_t max_group_size, int32_t max_group_levels, void* workspace,
+                                               size_t workspace_bytes, uint32_t* device_error, ra_stream_t stream) {
+  ra::clear_error();
+  if (!k_new || !v_new || !out_cache_loc)
+    return ra::fail(RA_ERR_INVALID_ARGUMENT, "k_new, v_new and out_cache_loc must all be non-null");
+  return decode_call(k_pool, v_pool, num_slots, num_kv_heads, head_dim, k_new, v_new, out_cache_loc, q, o,
+                     num_q_heads, sm_scale, req_to_token, table_stride, table_rows, req_pool_indices, seq_lens, batch,
+                     max_seq_len, num_groups, group_indptr, group_reqs, group_prefix_start, group_prefix_len,
+                     group_level, max_group_prefix_len, max_group_size, max_group_levels, workspace, workspace_bytes,
+                     device_error, stream);
 }

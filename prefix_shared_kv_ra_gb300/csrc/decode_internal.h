@@ -51,6 +51,12 @@ struct DecodeParams {
   float* casc_o;        // [batch, hq, casc_slots, D] shared-prefix partials (cascade)
   float* casc_lse;      // [batch, hq, casc_slots]; -inf marks a slot no group wrote
   uint32_t* err;
+  // fused store (ra_decode_attention_store): the step's new rows, scattered by the call's first kernel
+  const uint4* st_k;       // [batch, hkv, D] bf16 as 16-byte vectors, or nullptr (no store)
+  const uint4* st_v;
+  const int32_t* st_loc;   // [batch] destination slots
+  int32_t st_row_vecs;     // 16-byte vectors per slot row (hkv * D * 2 / 16)
+  int64_t st_total;        // batch * st_row_vecs
 };
 
 // The private keys of a decode call are cut into items on the device (decode_plan_kernel): at most

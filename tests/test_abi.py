@@ -28,7 +28,8 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for n in ("ra_kv_store", "ra_extend_attention", "ra_extend_workspace_bytes", "ra_decode_attention",
-              "ra_decode_workspace_bytes", "ra_status_string", "ra_last_error_message", "ra_abi_version"):
+              "ra_decode_workspace_bytes", "ra_decode_attention_store", "ra_status_string",
+              "ra_last_error_message", "ra_abi_version"):
         assert n in names
 
 
@@ -43,7 +44,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert ra.ra_abi_version() == 3
+    assert ra.ra_abi_version() == 4
     assert lib.ra_status_string(0) == b"ok"
     assert lib.ra_status_string(3) == b"workspace too small"
 
@@ -57,6 +58,25 @@ def _decode_call(lib, **over):
                 gp=None, gl=None, mgp=0, mgs=0, mgl=1, ws=FAKE, wsb=1 << 30, err=None, stream=None)
     args.update(over)
     return lib.ra_decode_attention(*args.values())
+
+
+def _store_decode_call(lib, kn=FAKE, vn=FAKE, loc=FAKE, **over):
+    args = dict(k=FAKE, v=FAKE, S=1024, hkv=8, d=128, kn=kn, vn=vn, loc=loc, q=FAKE, o=FAKE, hq=32, scale=0.088,
+                table=FAKE, stride=4096, rows=64, rpi=FAKE, lens=FAKE, batch=4, max_len=4096, ng=0, gi=None, gr=None,
+                gs=None, gp=None, gl=None, mgp=0, mgs=0, mgl=1, ws=FAKE, wsb=1 << 30, err=None, stream=None)
+    args.update(over)
+    return lib.ra_decode_attention_store(*args.values())
+
+
+def test_store_decode_validation(lib):
+    """The fused store + decode checks the store's arguments as well as the decode's; nothing launches."""
+    assert _store_decode_call(lib, kn=None) == 1                                   # missing new rows
+    assert _store_decode_call(lib, loc=None) == 1
+    assert _store_decode_call(lib, vn=ctypes.c_void_p((1 << 20) + 8)) == 1         # misaligned v_new
+    assert _store_decode_call(lib, loc=ctypes.c_void_p((1 << 20) + 2)) == 1        # misaligned slots
+    assert _store_decode_call(lib, hq=30) == 1                                     # decode checks still apply
+    assert _store_decode_call(lib, wsb=16) == 3
+    assert _store_decode_call(lib, batch=0) == 0                                   # empty batch: no-op
 
 
 def test_decode_validation(lib):

@@ -180,3 +180,55 @@ def test_decode_empty_batch_is_noop():
     ra.ra_decode_attention(db.k_pool, db.v_pool, db.dec_q[:0], db.dec_o[:0], db.table, db.dec_rpi[:0],
                            db.dec_lens[:0], max_seq_len=b.max_seq_len, sm_scale=b.sm_scale, workspace=ws)
     torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------- fused store + decode
+def _store_decode(db: DeviceBatch, cascade: bool):
+    b = db.b
+    kw = {}
+    if cascade:
+        kw = dict(group_indptr=db.g_indptr, group_reqs=db.g_reqs, group_prefix_len=db.g_plen,
+                  max_group_prefix_len=int(b.casc_group_prefix_len.max()),
+                  max_group_size=int(np.diff(b.casc_group_indptr).max()), group_prefix_start=db.g_start,
+                  group_level=db.g_level, max_group_levels=b.casc_levels)
+    ra.ra_decode_attention_store(db.k_pool, db.v_pool, db.k_new, db.v_new, db.loc, db.dec_q, db.dec_o, db.table,
+                                 db.dec_rpi, db.dec_lens, max_seq_len=b.max_seq_len, sm_scale=b.sm_scale,
+                                 workspace=db.decode_ws(cascade), device_error=db.err, **kw)
+
+
+@pytest.mark.parametrize("case,cascade", [("cfg2_decode_8b", False), ("cfg2_decode_8b", True),
+                                          ("cfg4_forked_decode_70b", True), ("random_large", False),
+                                          ("random_large", True)])
+def test_store_decode_fused_matches_store_then_decode(case, cascade):
+    """ra_decode_attention_store writes the same pool rows as ra_kv_store (bit-exact) and returns the same
+    outputs as ra_kv_store followed by ra_decode_attention (bit-exact: the same kernels read the same
+    pool), within the tolerance of the oracle."""
+    if case == "random_large":
+        b = W.random_mixed(34, n_extend=0, n_decode=2000, num_q_heads=8, num_kv_heads=2, head_dim=128, max_len=60,
+                           with_cascade=True)
+    else:
+        b = W.CONFIGS[case]()
+    assert b.n_extend == 0 and b.num_new_tokens == b.n_decode
+    ref = DeviceBatch(b)
+    ref.store()
+    ref.decode(cascade=cascade)
+    fused = DeviceBatch(b)
+    _store_decode(fused, cascade)
+    torch.cuda.synchronize()
+    assert int(ref.err.item()) == 0 and int(fused.err.item()) == 0
+    slots = b.out_cache_loc.astype(np.int64)
+    np.testing.assert_array_equal(_pool_rows(fused.k_pool, slots), b.k_new)
+    np.testing.assert_array_equal(_pool_rows(fused.v_pool, slots), b.v_new)
+    np.testing.assert_array_equal(fused.dec_o.view(torch.int16).cpu().numpy(), ref.dec_o.view(torch.int16).cpu().numpy())
+    if case == "random_large":
+        assert_close(to_f64(fused.dec_o).reshape(-1, b.head_dim), oracle.decode_batch(b), f"{b.name} fused decode")
+
+
+def test_store_decode_fused_bad_slot_is_flagged():
+    b = W.random_mixed(35, n_extend=0, n_decode=4, num_q_heads=8, num_kv_heads=2, head_dim=64, max_len=30)
+    db = DeviceBatch(b)
+    db.loc = torch.full_like(db.loc, b.num_slots + 5)  # every new row outside the pool: skipped, flagged
+    _store_decode(db, False)
+    torch.cuda.synchronize()
+    assert int(db.err.item()) & ra.DEVERR_SLOT
+
