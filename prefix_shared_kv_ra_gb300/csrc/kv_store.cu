@@ -23,20 +23,36 @@ __global__ void __launch_bounds__(256) kv_store_kernel(uint4* __restrict__ k_poo
                                                        uint32_t* __restrict__ err) {
   griddep_wait();  // earlier kernels may still read the pool rows this store overwrites
   griddep_launch();
+  // kU vectors of K and of V per thread and step, all loads issued before the stores (bytes in flight)
+  constexpr int kU = 4;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_vecs; i += stride) {
-    const int64_t tok = i / row_vecs;
-    const int32_t c = static_cast<int32_t>(i - tok * row_vecs);
-    const int32_t slot = __ldg(loc + tok);
-    if (slot < 0 || slot >= num_slots) {
-      if (c == 0) flag_error(err, RA_DEVERR_SLOT);
-      continue;
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < total_vecs;
+       i0 += kU * stride) {
+    uint4 kv[kU], vv[kU];
+    int32_t slot[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < total_vecs) {
+        slot[u] = __ldg(loc + i / row_vecs);
+        kv[u] = __ldg(k_new + i);
+        vv[u] = __ldg(v_new + i);
+      }
     }
-    const uint4 kv = __ldg(k_new + i);
-    const uint4 vv = __ldg(v_new + i);
-    const int64_t dst = static_cast<int64_t>(slot) * row_vecs + c;
-    k_pool[dst] = kv;
-    v_pool[dst] = vv;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i >= total_vecs) break;
+      const int64_t tok = i / row_vecs;
+      const int32_t c = static_cast<int32_t>(i - tok * row_vecs);
+      if (slot[u] < 0 || slot[u] >= num_slots) {
+        if (c == 0) flag_error(err, RA_DEVERR_SLOT);
+        continue;
+      }
+      const int64_t dst = static_cast<int64_t>(slot[u]) * row_vecs + c;
+      k_pool[dst] = kv[u];
+      v_pool[dst] = vv[u];
+    }
   }
 }
 
@@ -64,7 +80,7 @@ extern "C" ra_status ra_kv_store(void* k_pool, void* v_pool, int64_t num_slots, 
   const int32_t row_vecs = static_cast<int32_t>(row_bytes / 16);
   const int64_t total = num_tokens * row_vecs;
   const int threads = 256;
-  const int64_t want = (total + threads - 1) / threads;
+  const int64_t want = (total + threads * 4 - 1) / (threads * 4);  // 4 vectors per thread
   const int64_t cap = static_cast<int64_t>(dev.num_sms) * 8;
   const int blocks = static_cast<int>(want < cap ? want : cap);
   return launch_pdl("kv_store_kernel", kv_store_kernel, dim3(blocks), dim3(threads), 0,
