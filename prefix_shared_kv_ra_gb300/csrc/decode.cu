@@ -695,7 +695,6 @@ static int32_t heads_per_cta(int32_t num_kv_heads) {
 DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seq_len,
                        int32_t num_groups, int32_t max_group_prefix_len, int32_t max_group_size) {
   DecodePlan pl;
-  (void)max_seq_len;
   pl.max_items = kDecodePlanItems + batch;
   if (num_groups > 0 && max_group_prefix_len > 0) {
     // Prefix keys per prefix-pass CTA (a multiple of the 128-key tile, at most 2048): the split count
@@ -706,10 +705,14 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
     const int64_t mtiles = (max_group_size + members_per_cta - 1) / members_per_cta;
     const int64_t base = static_cast<int64_t>(num_groups) * num_kv_heads * mtiles;
     const int64_t tiles = (max_group_prefix_len + 127) / 128;
-    // CTAs per wave: two thirds of GB300's 152 SMs, the rest run the private decode beside the pass.
-    // A constant: the workspace size (sized on the host, possibly with no device current) must not
-    // depend on which device runs the call; only the split balance does.
-    constexpr int64_t sms = 104;
+    // CTAs per wave: GB300's 152 SMs in the share the shared prefix takes of the longest context (the
+    // host-side bounds), at least two thirds of them; the rest run the private decode beside the pass.
+    // Measured: a forked batch (8192 shared + <= 257 private keys) 64 -> 58 us with all SMs for the
+    // pass, while the 8B-shape batch (1024 shared of <= 4096) loses 10% unless a third is left to its
+    // private keys.  Computed from the call's bounds, not the device: the workspace size (sized on the
+    // host, possibly with no device current) must not depend on which device runs the call.
+    const int64_t share = 152 * static_cast<int64_t>(max_group_prefix_len) / (max_seq_len > 0 ? max_seq_len : 1);
+    const int64_t sms = share < 104 ? 104 : (share > 152 ? 152 : share);
     int64_t best_tiles = 16, best_cost = -1;
     for (int64_t per = 16; per >= 1; --per) {  // tiles per CTA
       const int64_t splits = (tiles + per - 1) / per;
