@@ -144,7 +144,10 @@ size_t ra_extend_workspace_bytes(int32_t batch, int64_t total_q, int32_t num_q_h
  *   q, o:     bf16 [batch, num_q_heads, head_dim]; o must not alias q or the pools.
  *   seq_lens: int32 [batch]; max_seq_len is its host-side upper bound.
  * Key ranges are split across CTAs (split-KV) and merged with a log-sum-exp
- * combine pass; the partial results live in `workspace`.
+ * combine pass; the partial results live in `workspace`.  The split is planned
+ * on the device from the actual lengths: at most 456 equal items (>= 128 keys)
+ * plus one shorter item per request, so the workspace is bounded by
+ * (456 + batch) partial rows per q head whatever max_seq_len is.
  *
  * Optional prefix-grouped (cascade) read, num_groups > 0: group g lists
  * decode requests group_reqs[group_indptr[g] .. group_indptr[g+1]) whose table
