@@ -494,14 +494,6 @@ __device__ __forceinline__ void plan_scan2(int32_t& a, int32_t& b, int32_t& ta, 
   __syncthreads();  // the scratch may be reused
 }
 
-// The private-key work plan of one decode call, made on the device from the real lengths (the host only
-// knows bounds).  T = the batch's private keys (seq_len minus the cascade start, over valid requests);
-// chunk = max(kDecodeMinChunk, T / kDecodePlanItems rounded up to 16), so a call has at most
-// kDecodePlanItems + batch items however long its contexts are.  Request b's items get the dense indices
-// req_item0[b] .. req_item0[b+1]-1 (where their partials live); the claim order lists every full-chunk
-// item first, then each request's shorter last item by decreasing size (longest processing time first),
-// so the CTAs that finish last finish on short items.  One CTA of kPlanThreads threads; each thread owns
-// a contiguous run of requests.  It also resets the work counter.
 // Fused store (ra_decode_attention_store): pool[st_loc[b]] = new row b for K and V, one 16-byte vector
 // per thread and step, consecutive threads on consecutive vectors of a row (as ra_kv_store).  Run by
 // the call's first kernel after it waited for the kernels before it (they may still read the slots).
@@ -523,6 +515,15 @@ __device__ __forceinline__ void scatter_new_rows(const DecodeParams& p, int64_t 
   }
 }
 
+// The private-key work plan of one decode call, made on the device from the real lengths (the host only
+// knows bounds).  T = the batch's private keys (seq_len minus the cascade start, over valid requests);
+// chunk = max(kDecodeMinChunk, T / kDecodePlanItems rounded up to 16), so a call has at most
+// kDecodePlanItems + batch items however long its contexts are.  Request b's items get the dense indices
+// req_item0[b] .. req_item0[b+1]-1 (where their partials live); the claim order lists every full-chunk
+// item first, then each request's shorter last item by decreasing size (longest processing time first),
+// so the CTAs that finish last finish on short items.  One CTA of kPlanThreads threads; each thread owns
+// a contiguous run of requests.  It also resets the work counter.  With a fused store (and no groups)
+// CTAs 1.. of the grid scatter the step's new rows instead.
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeParams p) {
   if (blockIdx.x > 0) {  // the fused store's CTAs (only without groups; CTA 0 plans)
     griddep_launch();
