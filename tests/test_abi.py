@@ -152,3 +152,22 @@ def test_binding_refuses_to_run_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_build, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         ra.load()
+
+
+def test_store_decode_binding_checks_shapes_before_the_call():
+    """The Python binding of the fused store + decode rejects new rows or slots of the wrong shape, and
+    tensors of the wrong dtype, before anything reaches the library (CPU tensors: no launch)."""
+    import torch
+    pool = torch.zeros((64, 2, 64), dtype=torch.bfloat16)
+    q = torch.zeros((3, 8, 64), dtype=torch.bfloat16)
+    table = torch.zeros((3, 16), dtype=torch.int32)
+    idx = torch.zeros(3, dtype=torch.int32)
+    ws = torch.zeros(256, dtype=torch.uint8)
+    args = dict(max_seq_len=16, sm_scale=0.125, workspace=ws)
+    kn = torch.zeros((3, 2, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):  # one new row per request
+        ra.ra_decode_attention_store(pool, pool, kn[:2], kn[:2], idx[:2], q, q.clone(), table, idx, idx, **args)
+    with pytest.raises(ValueError):  # out_cache_loc has one entry per request
+        ra.ra_decode_attention_store(pool, pool, kn, kn, idx[:1], q, q.clone(), table, idx, idx, **args)
+    with pytest.raises(TypeError):  # slots are int32
+        ra.ra_decode_attention_store(pool, pool, kn, kn, idx.long(), q, q.clone(), table, idx, idx, **args)
