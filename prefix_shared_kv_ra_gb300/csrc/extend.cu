@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kPlanThreads) extend_plan_kernel(const int32_t
   __shared__ int32_t s_bin[kPlanBins];
   __shared__ int32_t s_warp[kPlanThreads / 32];
   griddep_launch();  // the extend kernel may start its launch; it waits for this grid before reading the list
+  // (this grid waits for the previous one before its first write, so its completion implies that one's)
   for (int i = threadIdx.x; i < kPlanBins; i += kPlanThreads) s_bin[i] = 0;
   __syncthreads();
   // a request's tiles, or 0 if its lengths are invalid (flagged here, once)
@@ -123,6 +124,9 @@ __global__ void __launch_bounds__(kPlanThreads) extend_plan_kernel(const int32_t
 #pragma unroll
   for (int e = 0; e < kPer; ++e) s_bin[threadIdx.x * kPer + e] = base + v[e];
   __syncthreads();
+  // Everything above read only the call's inputs.  The writes below wait for the previous kernel: it may
+  // be the previous call's extend kernel on this workspace, still claiming from its list and counter.
+  griddep_wait();
   for (int b = threadIdx.x; b < batch; b += kPlanThreads) {
     int32_t P, E;
     const int32_t n = tiles_of(b, P, E, false);
@@ -140,7 +144,6 @@ __global__ void __launch_bounds__(kPlanThreads) extend_plan_kernel(const int32_t
     *count = static_cast<int32_t>(static_cast<int64_t>(total) < cap ? total : cap);
     *counter = 0;
   }
-  griddep_wait();  // complete only after the previous grid (the KV store): the extend kernel waits on this one
 }
 
 // K ring / V ring depths: the tensor core waits on K first, so K gets the deeper ring.
