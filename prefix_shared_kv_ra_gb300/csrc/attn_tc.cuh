@@ -126,6 +126,11 @@ struct Layout {
 
 __device__ __forceinline__ bool aborted(volatile int* flag) { return *flag != 0; }
 
+template <bool B>
+struct BoolTag {
+  static constexpr bool value = B;
+};
+
 // One work item: key range, table row and query rows.
 struct Job {
   int32_t kh;
@@ -602,6 +607,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         tc_fence_after();
         const int32_t key0 = jb.kbeg + j * kKeys;
         const bool masked = key0 + kKeys > lim;
+        const bool warp_masked = __any_sync(0xffffffffu, masked);
         // Every tile is exponentiated against a reference in a single pass: the current one, or on the
         // item's first tile the maximum of its first 32 columns.  The row sum bounds every probability
         // of the row (p <= sum), so a sum above kFastSumLimit, or one that is not finite, marks the
@@ -661,11 +667,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
           const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
           const uint64_t neg_m2 = f2_pack(-m_sub, -m_sub);
           uint64_t sum2[4] = {0, 0, 0, 0};  // 4 independent chains of (even, odd) partial sums
-          auto exp_chunk = [&](const uint32_t (&sr)[32], int c) {
+          // The causal / range mask is compiled only into the variant a warp takes when one of its rows
+          // ends inside this tile: the other tiles issue no compare or select per score.
+          auto exp_chunk = [&](const uint32_t (&sr)[32], int c, auto mask_tag) {
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
               float s0 = __uint_as_float(sr[2 * e]), s1 = __uint_as_float(sr[2 * e + 1]);
-              if (masked) {
+              if constexpr (decltype(mask_tag)::value) {
                 if (key0 + c * 32 + 2 * e >= lim) s0 = -INFINITY;
                 if (key0 + c * 32 + 2 * e + 1 >= lim) s1 = -INFINITY;
               }
@@ -676,21 +684,23 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
               pk[c >> 1][(c & 1) * 16 + e] = pack_bf16x2(p0, p1);
             }
           };
-          {
+          auto exp_tile = [&](auto mask_tag) {
             uint32_t ba[32], bb[32];
             tmem_ld32(tmem + lane_addr + col_s, ba);
             tc_wait_ld_regs(ba);
             tmem_ld32(tmem + lane_addr + col_s + 32, bb);
-            exp_chunk(ba, 0);
+            exp_chunk(ba, 0, mask_tag);
             tc_wait_ld_regs(bb);
             tmem_ld32(tmem + lane_addr + col_s + 64, ba);
-            exp_chunk(bb, 1);
+            exp_chunk(bb, 1, mask_tag);
             tc_wait_ld_regs(ba);
             tmem_ld32(tmem + lane_addr + col_s + 96, bb);
-            exp_chunk(ba, 2);
+            exp_chunk(ba, 2, mask_tag);
             tc_wait_ld_regs(bb);
-            exp_chunk(bb, 3);
-          }
+            exp_chunk(bb, 3, mask_tag);
+          };
+          if (warp_masked) exp_tile(BoolTag<true>{});
+          else exp_tile(BoolTag<false>{});
           float sum8[8];
 #pragma unroll
           for (int e = 0; e < 4; ++e) f2_unpack(sum2[e], sum8[2 * e], sum8[2 * e + 1]);
