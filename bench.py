@@ -369,10 +369,10 @@ def extra_kernels(dev, flush, peaks, reps: int = 20):
     """The same kernels on the other workloads (parity-tested elsewhere): per-kernel roofline."""
     import workloads as W
     out = {}
-    specs = [("decode_8b_system_prompts", W.cfg2_decode_8b, (False, True)),
-             ("decode_8b_system_prompts_page16", lambda: W.cfg2_decode_8b(page_size=16), (False,)),
-             ("extend_fewshot_3000", W.cfg3_fewshot_extend, (False,)),
-             ("decode_70b_forked_8192", W.cfg4_forked_decode_70b, (False, True))]
+    specs = [("decode_8b_system_prompts", W.decode_8b_system_prompts, (False, True)),
+             ("decode_8b_system_prompts_page16", lambda: W.decode_8b_system_prompts(page_size=16), (False,)),
+             ("extend_fewshot_3000", W.fewshot_extend, (False,)),
+             ("decode_70b_forked_8192", W.forked_decode_70b, (False, True))]
     for name, fn, modes in specs:
         b = fn()
         for casc in modes:
@@ -397,7 +397,7 @@ def extra_kernels(dev, flush, peaks, reps: int = 20):
             del st
     # the decode step's store fused into the decode call, against the two calls (whole steps, no events
     # between the calls, so the programmatic launch chain is kept in both)
-    b = W.cfg2_decode_8b()
+    b = W.decode_8b_system_prompts()
     steps = {}
     for fused in (False, True):
         st = Step(b, dev, fused_store=fused)
@@ -477,7 +477,7 @@ def oracle_sample(b, budget_s: float, seed: int = 0):
 
 def run_reference(args):
     import workloads as W
-    b = W.cfg5_multiturn_mix_70b()
+    b = W.multiturn_mix_70b()
     res = [oracle_sample(b, args.ref_budget, seed=k) for k in range(args.warmup + args.steps)]
     timed = res[args.warmup:]
     val = float(np.mean([r["value"] for r in timed]))
@@ -495,12 +495,12 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- ncu cases
 PROFILE_CASES = {
-    "extend_fewshot": ("cfg3_fewshot_extend", False),
-    "multiturn_mix_cascade": ("cfg5_multiturn_mix_70b", True),
-    "decode_8b": ("cfg2_decode_8b", False),
-    "decode_8b_cascade": ("cfg2_decode_8b", True),
-    "decode_70b_forked_cascade": ("cfg4_forked_decode_70b", True),
-    "multiturn_mix": ("cfg5_multiturn_mix_70b", False),
+    "extend_fewshot": ("fewshot_extend", False),
+    "multiturn_mix_cascade": ("multiturn_mix_70b", True),
+    "decode_8b": ("decode_8b_system_prompts", False),
+    "decode_8b_cascade": ("decode_8b_system_prompts", True),
+    "decode_70b_forked_cascade": ("forked_decode_70b", True),
+    "multiturn_mix": ("multiturn_mix_70b", False),
 }
 
 
@@ -512,7 +512,7 @@ def run_profile_case(name: str, steps: int):
     ra.load()
     cfg, cascade = PROFILE_CASES[name]
     dev = torch.device("cuda:0")
-    b = W.CONFIGS[cfg]()
+    b = W.WORKLOADS[cfg]()
     if cascade and not b.has_cascade():
         b = with_tree_groups(b)
     st = Step(b, dev, cascade=cascade)
@@ -581,7 +581,7 @@ def main():
 
     # independent replicas: each rank draws its own batch of the same workload; the decode requests are
     # grouped by the radix tree (one-level cascade groups over shared prefixes of >= 256 tokens)
-    b = with_tree_groups(W.cfg5_multiturn_mix_70b(seed=5 + rank))
+    b = with_tree_groups(W.multiturn_mix_70b(seed=5 + rank))
     step = Step(b, dev, cascade=True)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     uuid = None

@@ -26,7 +26,7 @@ def check_extend(db: DeviceBatch, sel=None):
 
 
 def test_extend_tiny_config():
-    e, _ = W.cfg1_tiny()
+    e, _ = W.tiny_extend_decode()
     db = DeviceBatch(e)
     db.store()
     check_extend(db)
@@ -106,7 +106,7 @@ def test_chunked_prefill(chunk):
 
 
 def test_extend_fewshot_full():
-    b = W.cfg3_fewshot_extend()
+    b = W.fewshot_extend()
     db = DeviceBatch(b)
     db.store()
     rng = np.random.default_rng(3)
@@ -116,7 +116,7 @@ def test_extend_fewshot_full():
 
 
 def test_extend_multiturn_mix_sampled():
-    b = W.cfg5_multiturn_mix_70b()
+    b = W.multiturn_mix_70b()
     db = DeviceBatch(b)
     db.store()
     rng = np.random.default_rng(4)
@@ -175,7 +175,7 @@ def check_cascade(db: DeviceBatch, sel=None):
 
 
 def test_cascade_tiny_config():
-    _, d = W.cfg1_tiny()
+    _, d = W.tiny_extend_decode()
     db = DeviceBatch(d)
     db.store()
     check_cascade(db)
@@ -193,9 +193,9 @@ def test_cascade_ragged(seed, hq, hkv, d, max_len):
     check_cascade(db)
 
 
-@pytest.mark.parametrize("name", ["cfg2_decode_8b", "cfg4_forked_decode_70b"])
+@pytest.mark.parametrize("name", ["decode_8b_system_prompts", "forked_decode_70b"])
 def test_cascade_full_workloads(name):
-    b = W.CONFIGS[name]()
+    b = W.WORKLOADS[name]()
     db = DeviceBatch(b)
     db.store()
     check_cascade(db)
@@ -217,7 +217,7 @@ def test_cascade_member_without_private_keys():
 
 def test_cascade_multiturn_mix_tree_groups_sampled():
     """The multi-turn mix's decode with one-level groups derived by the radix tree (prefixes up to ~14K)."""
-    b = attach_tree_groups(W.cfg5_multiturn_mix_70b())
+    b = attach_tree_groups(W.multiturn_mix_70b())
     assert b.has_cascade()
     db = DeviceBatch(b)
     db.store()
@@ -228,7 +228,7 @@ def test_cascade_multiturn_mix_tree_groups_sampled():
 
 def test_cascade_growing_scores():
     """The prefix pass's tiles (several per split) under scores that grow tile by tile."""
-    b = grow_key_scale(W.cfg2_decode_8b())  # 8 groups sharing 1024 prompt tokens: 512-key splits of 4 tiles
+    b = grow_key_scale(W.decode_8b_system_prompts())  # 8 groups sharing 1024 prompt tokens: 512-key splits of 4 tiles
     assert b.has_cascade()
     db = DeviceBatch(b)
     db.store()
@@ -247,7 +247,7 @@ def test_cascade_multilevel_random(seed, hq, hkv, d):
 
 
 def test_cascade_multilevel_multiturn_mix_sampled():
-    b = attach_tree_groups_multilevel(W.cfg5_multiturn_mix_70b())
+    b = attach_tree_groups_multilevel(W.multiturn_mix_70b())
     assert b.casc_levels >= 2
     db = DeviceBatch(b)
     db.store()

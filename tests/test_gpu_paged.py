@@ -24,7 +24,7 @@ def test_paged_store_extend_decode(seed, hq, hkv, d):
 
 
 def test_paged_decode_8b_cascade():
-    b = W.cfg2_decode_8b(page_size=16)
+    b = W.decode_8b_system_prompts(page_size=16)
     assert b.has_cascade()
     db = DeviceBatch(b)
     db.store()

@@ -53,7 +53,7 @@ def check_decode(db: DeviceBatch, sel=None, cascade=False):
 
 # ---------------------------------------------------------------- store
 def test_store_tiny_bit_exact():
-    e, d = W.cfg1_tiny()
+    e, d = W.tiny_extend_decode()
     for b in (e, d):
         db = DeviceBatch(b)
         db.store()
@@ -65,10 +65,10 @@ def test_store_tiny_bit_exact():
         np.testing.assert_array_equal(got_v, v_ref)
 
 
-@pytest.mark.parametrize("name", ["cfg2_decode_8b", "cfg3_fewshot_extend", "cfg4_forked_decode_70b",
-                                  "cfg5_multiturn_mix_70b"])
+@pytest.mark.parametrize("name", ["decode_8b_system_prompts", "fewshot_extend", "forked_decode_70b",
+                                  "multiturn_mix_70b"])
 def test_store_full_workloads(name):
-    check_store(DeviceBatch(W.CONFIGS[name]()))
+    check_store(DeviceBatch(W.WORKLOADS[name]()))
 
 
 def test_store_empty_and_bad_slot_flag():
@@ -89,7 +89,7 @@ def test_store_empty_and_bad_slot_flag():
 
 # ---------------------------------------------------------------- decode
 def test_decode_tiny_config():
-    _, d = W.cfg1_tiny()
+    _, d = W.tiny_extend_decode()
     db = DeviceBatch(d)
     db.store()
     check_decode(db)
@@ -143,16 +143,16 @@ def test_decode_single_token_contexts():
     np.testing.assert_array_equal(got, np.repeat(v, 4, axis=1))
 
 
-@pytest.mark.parametrize("name", ["cfg2_decode_8b", "cfg4_forked_decode_70b"])
+@pytest.mark.parametrize("name", ["decode_8b_system_prompts", "forked_decode_70b"])
 def test_decode_full_workloads(name):
-    b = W.CONFIGS[name]()
+    b = W.WORKLOADS[name]()
     db = DeviceBatch(b)
     db.store()
     check_decode(db)
 
 
 def test_decode_multiturn_mix_sampled():
-    b = W.cfg5_multiturn_mix_70b()
+    b = W.multiturn_mix_70b()
     db = DeviceBatch(b)
     db.store()
     rng = np.random.default_rng(1)
@@ -196,8 +196,8 @@ def _store_decode(db: DeviceBatch, cascade: bool):
                                  workspace=db.decode_ws(cascade), device_error=db.err, **kw)
 
 
-@pytest.mark.parametrize("case,cascade", [("cfg2_decode_8b", False), ("cfg2_decode_8b", True),
-                                          ("cfg4_forked_decode_70b", True), ("random_large", False),
+@pytest.mark.parametrize("case,cascade", [("decode_8b_system_prompts", False), ("decode_8b_system_prompts", True),
+                                          ("forked_decode_70b", True), ("random_large", False),
                                           ("random_large", True)])
 def test_store_decode_fused_matches_store_then_decode(case, cascade):
     """ra_decode_attention_store writes the same pool rows as ra_kv_store (bit-exact) and returns the same
@@ -207,7 +207,7 @@ def test_store_decode_fused_matches_store_then_decode(case, cascade):
         b = W.random_mixed(34, n_extend=0, n_decode=2000, num_q_heads=8, num_kv_heads=2, head_dim=128, max_len=60,
                            with_cascade=True)
     else:
-        b = W.CONFIGS[case]()
+        b = W.WORKLOADS[case]()
     assert b.n_extend == 0 and b.num_new_tokens == b.n_decode
     ref = DeviceBatch(b)
     ref.store()

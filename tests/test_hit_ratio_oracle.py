@@ -67,7 +67,7 @@ def test_generator_construction_ratio_matches_definition_small():
 
 
 def test_multiturn_mix_hit_ratio_is_seventy_percent():
-    b = W.cfg5_multiturn_mix_70b()
+    b = W.multiturn_mix_70b()
     hr = H.hit_ratio(b.tokens)
     assert abs(hr - 0.70) <= 0.01
     assert hr == pytest.approx(b.meta["construction_hit_ratio"], abs=1e-12)

@@ -31,7 +31,7 @@ def test_oracle_matches_brute_force(seed, hq, hkv, d):
 
 
 def test_oracle_matches_brute_force_tiny_config():
-    e, d = W.cfg1_tiny()
+    e, d = W.tiny_extend_decode()
     np.testing.assert_allclose(oracle.extend_batch(e), np.array(brute.extend(e)), rtol=0, atol=1e-12)
     np.testing.assert_allclose(oracle.decode_batch(d), np.array(brute.decode(d)), rtol=0, atol=1e-12)
 

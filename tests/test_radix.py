@@ -87,7 +87,7 @@ def test_eviction_respects_locks_lru_and_returns_slots():
 
 
 def test_cascade_groups_share_their_prefix_slots():
-    b = W.cfg2_decode_8b()
+    b = W.decode_8b_system_prompts()
     rows = [b.req_to_token[r, :L] for r, L in zip(b.dec_rpi, b.dec_seq_lens)]
     gi, gr, gp = cascade_groups(rows)
     assert gi.size - 1 == 8  # one group per system prompt
@@ -209,7 +209,7 @@ def test_multilevel_groups_are_the_shared_nodes_of_the_rows():
 
 def test_multilevel_groups_on_a_generated_batch():
     from prefix_shared_kv_ra_gb300.radix import cascade_groups_multilevel
-    b = W.cfg5_multiturn_mix_70b()
+    b = W.multiturn_mix_70b()
     rows = [b.req_to_token[r, :L] for r, L in zip(b.dec_rpi, b.dec_seq_lens)]
     indptr, reqs, start, end, level, nl = cascade_groups_multilevel(rows)
     assert nl >= 2 and len(start) > 0

@@ -34,7 +34,7 @@ def _check_batch(b):
 
 
 def test_tiny_config_shapes():
-    e, d = W.cfg1_tiny()
+    e, d = W.tiny_extend_decode()
     assert list(e.ext_extend_lens) == [8, 12, 16, 24] and list(e.ext_prefix_lens) == [32] * 4
     assert (e.num_q_heads, e.num_kv_heads, e.head_dim, e.num_slots) == (8, 2, 64, 512)
     assert list(d.dec_seq_lens) == [41, 45, 49, 57]
@@ -46,18 +46,18 @@ def test_tiny_config_shapes():
     _check_batch(d)
 
 
-@pytest.mark.parametrize("name", ["cfg2_decode_8b", "cfg3_fewshot_extend", "cfg4_forked_decode_70b"])
+@pytest.mark.parametrize("name", ["decode_8b_system_prompts", "fewshot_extend", "forked_decode_70b"])
 def test_config_invariants(name):
-    b = W.CONFIGS[name]()
+    b = W.WORKLOADS[name]()
     _check_batch(b)
-    if name == "cfg2_decode_8b":
+    if name == "decode_8b_system_prompts":
         assert b.n_decode == 64 and (b.num_q_heads, b.num_kv_heads, b.head_dim) == (32, 8, 128)
         assert b.dec_seq_lens.min() >= 512 and b.dec_seq_lens.max() <= 4096
         assert b.casc_group_indptr.size == 9
-    if name == "cfg3_fewshot_extend":
+    if name == "fewshot_extend":
         assert b.n_extend == 16 and np.all(b.ext_prefix_lens == 3000)
         assert b.ext_extend_lens.min() >= 200 and b.ext_extend_lens.max() <= 400
-    if name == "cfg4_forked_decode_70b":
+    if name == "forked_decode_70b":
         assert b.n_decode == 64 and (b.num_q_heads, b.num_kv_heads) == (64, 8)
         assert np.all((b.dec_seq_lens >= 8193) & (b.dec_seq_lens <= 8192 + 257))
         assert list(b.casc_group_prefix_len) == [8192]

@@ -54,7 +54,7 @@ def _reference(db: DeviceBatch, cascade: bool) -> np.ndarray:
 
 def test_static_scratch_decode_matches_workspace_decode_on_two_calls():
     cases = [
-        (DeviceBatch(W.cfg2_decode_8b()), True),   # system-prompt groups, cascade prefix pass + splits
+        (DeviceBatch(W.decode_8b_system_prompts()), True),   # system-prompt groups, cascade prefix pass + splits
         (DeviceBatch(W.random_mixed(31, n_extend=0, n_decode=12, num_q_heads=32, num_kv_heads=8, head_dim=128,
                                     max_len=2500)), False),
     ]

@@ -30,8 +30,8 @@ import numpy as np
 
 __all__ = [
     "SeqSpec", "Batch", "build_batch", "f32_to_bf16_bits", "bf16_bits_to_f32",
-    "cfg1_tiny", "cfg2_decode_8b", "cfg3_fewshot_extend", "cfg4_forked_decode_70b",
-    "cfg5_multiturn_mix_70b", "random_mixed", "CONFIGS",
+    "tiny_extend_decode", "decode_8b_system_prompts", "fewshot_extend", "forked_decode_70b",
+    "multiturn_mix_70b", "random_mixed", "WORKLOADS",
 ]
 
 NO_SLOT = -1  # unused req_to_token entries; a kernel that reads one has a bug
@@ -295,7 +295,7 @@ def build_batch(name: str, specs: Sequence[SeqSpec], *, num_slots: int, num_q_he
 # ----------------------------------------------------------------------------
 # the five workloads
 # ----------------------------------------------------------------------------
-def cfg1_tiny(seed: int = 1) -> Tuple[Batch, Batch]:
+def tiny_extend_decode(seed: int = 1) -> Tuple[Batch, Batch]:
     """Tiny correctness case: 4 requests share a 32-token cached prefix, suffixes
     of 8/12/16/24 tokens, 8 q heads / 2 kv heads, head_dim 64, 512 slots.
 
@@ -305,7 +305,7 @@ def cfg1_tiny(seed: int = 1) -> Tuple[Batch, Batch]:
     """
     suffix = [8, 12, 16, 24]
     specs = [SeqSpec(32, 32, "cached")] + [SeqSpec(32 + e, 32, "extend", parent=0, fork=32) for e in suffix]
-    ext = build_batch("cfg1_tiny_extend", specs, num_slots=512, num_q_heads=8, num_kv_heads=2,
+    ext = build_batch("tiny_extend", specs, num_slots=512, num_q_heads=8, num_kv_heads=2,
                       head_dim=64, seed=seed)
     # decode step: same slots for the first 32+E positions, one new slot each
     rng = np.random.Generator(np.random.PCG64(seed + 1000))
@@ -322,7 +322,7 @@ def cfg1_tiny(seed: int = 1) -> Tuple[Batch, Batch]:
     for k in range(4):
         table[ext.ext_rpi[k], seq_lens[k] - 1] = new_slots[k]
     dec = Batch(
-        name="cfg1_tiny_decode", num_slots=512, num_q_heads=8, num_kv_heads=2, head_dim=64,
+        name="tiny_decode", num_slots=512, num_q_heads=8, num_kv_heads=2, head_dim=64,
         sm_scale=ext.sm_scale, pool_slots=pool_slots, pool_k=pool_k, pool_v=pool_v,
         out_cache_loc=new_slots, k_new=_normal_bf16(rng, (4, 2, 64)), v_new=_normal_bf16(rng, (4, 2, 64)),
         req_to_token=table,
@@ -336,7 +336,7 @@ def cfg1_tiny(seed: int = 1) -> Tuple[Batch, Batch]:
     return ext, dec
 
 
-def cfg2_decode_8b(seed: int = 2, page_size: int = 1) -> Batch:
+def decode_8b_system_prompts(seed: int = 2, page_size: int = 1) -> Batch:
     """Decode, Llama-3-8B attention shape: batch 64, 32 q / 8 kv heads, head_dim 128.
     Context lengths (including the new token) uniform in 512..4096; 8 groups of 8
     requests share a 1024-token system prompt (same slots); pool of 512K slots.
@@ -356,23 +356,23 @@ def cfg2_decode_8b(seed: int = 2, page_size: int = 1) -> Batch:
                 members.append(len(specs) - 1)
         if len(members) >= 2:
             groups.append((members, 1024))
-    return build_batch("cfg2_decode_8b" if page_size == 1 else f"cfg2_decode_8b_page{page_size}", specs,
-                       num_slots=512 * 1024, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=seed + 1,
+    name = "decode_8b_system_prompts" if page_size == 1 else f"decode_8b_system_prompts_page{page_size}"
+    return build_batch(name, specs, num_slots=512 * 1024, num_q_heads=32, num_kv_heads=8, head_dim=128, seed=seed + 1,
                        cascade=groups, page_size=page_size)
 
 
-def cfg3_fewshot_extend(seed: int = 3) -> Batch:
+def fewshot_extend(seed: int = 3) -> Batch:
     """Few-shot extend: 16 requests share a cached 3000-token prefix, each with
     200..400 new suffix tokens; 32 q / 8 kv heads, head_dim 128, scale 1/sqrt(128)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     ext = rng.integers(200, 400, size=16, endpoint=True)
     specs = [SeqSpec(3000, 3000, "cached")] + [
         SeqSpec(3000 + int(e), 3000, "extend", parent=0, fork=3000) for e in ext]
-    return build_batch("cfg3_fewshot_extend", specs, num_slots=64 * 1024, num_q_heads=32, num_kv_heads=8,
+    return build_batch("fewshot_extend", specs, num_slots=64 * 1024, num_q_heads=32, num_kv_heads=8,
                        head_dim=128, seed=seed + 1)
 
 
-def cfg4_forked_decode_70b(seed: int = 4) -> Batch:
+def forked_decode_70b(seed: int = 4) -> Batch:
     """Forked-branch decode, Llama-3-70B attention shape (64 q / 8 kv heads, D 128):
     one 8192-token shared prefix, 64 sibling branches with 0..256 private tokens
     each, then one decode token per branch (L = 8192 + p + 1).  One cascade group."""
@@ -382,11 +382,11 @@ def cfg4_forked_decode_70b(seed: int = 4) -> Batch:
     for p in priv:
         L = 8192 + int(p) + 1
         specs.append(SeqSpec(L, L - 1, "decode", parent=0, fork=8192))
-    return build_batch("cfg4_forked_decode_70b", specs, num_slots=64 * 1024, num_q_heads=64, num_kv_heads=8,
+    return build_batch("forked_decode_70b", specs, num_slots=64 * 1024, num_q_heads=64, num_kv_heads=8,
                        head_dim=128, seed=seed + 1, cascade=[(list(range(1, 65)), 8192)])
 
 
-def _cfg5_specs(lens: np.ndarray, is_ext: np.ndarray, ext_len: np.ndarray, u: np.ndarray,
+def _multiturn_mix_specs(lens: np.ndarray, is_ext: np.ndarray, ext_len: np.ndarray, u: np.ndarray,
                 pick: np.ndarray, alpha: float, window: int) -> Tuple[List[SeqSpec], float]:
     specs: List[SeqSpec] = []
     num = den = 0
@@ -406,7 +406,7 @@ def _cfg5_specs(lens: np.ndarray, is_ext: np.ndarray, ext_len: np.ndarray, u: np
     return specs, (num / den if den else 0.0)
 
 
-def cfg5_multiturn_mix_70b(seed: int = 5, target_hit: float = 0.70, num_slots: int = 2 * 1024 * 1024) -> Batch:
+def multiturn_mix_70b(seed: int = 5, target_hit: float = 0.70, num_slots: int = 2 * 1024 * 1024) -> Batch:
     """Multi-turn chat mix, 70B heads (64 / 8, D 128): 256 requests, contexts
     lognormal(median 2048, sigma 1) clipped to [16, 32768].  Sequences are generated
     in ascending length; with probability alpha a request continues or forks one of
@@ -427,15 +427,15 @@ def cfg5_multiturn_mix_70b(seed: int = 5, target_hit: float = 0.70, num_slots: i
     lo, hi = 0.0, 1.0
     for _ in range(40):
         mid = 0.5 * (lo + hi)
-        _, h = _cfg5_specs(lens, is_ext, ext_len, u, pick, mid, 8)
+        _, h = _multiturn_mix_specs(lens, is_ext, ext_len, u, pick, mid, 8)
         if h < target_hit:
             lo = mid
         else:
             hi = mid
     alpha = hi
-    specs, hit = _cfg5_specs(lens, is_ext, ext_len, u, pick, alpha, 8)
+    specs, hit = _multiturn_mix_specs(lens, is_ext, ext_len, u, pick, alpha, 8)
     assert abs(hit - target_hit) <= 0.01, hit
-    return build_batch("cfg5_multiturn_mix_70b", specs, num_slots=num_slots, num_q_heads=64, num_kv_heads=8,
+    return build_batch("multiturn_mix_70b", specs, num_slots=num_slots, num_q_heads=64, num_kv_heads=8,
                        head_dim=128, seed=seed + 1,
                        meta={"alpha": alpha, "construction_hit_ratio": hit})
 
@@ -507,9 +507,9 @@ def random_mixed(seed: int, *, n_extend: int, n_decode: int, num_q_heads: int, n
                        seed=seed + 7919, cascade=cascade, page_size=page_size)
 
 
-CONFIGS = {
-    "cfg2_decode_8b": cfg2_decode_8b,
-    "cfg3_fewshot_extend": cfg3_fewshot_extend,
-    "cfg4_forked_decode_70b": cfg4_forked_decode_70b,
-    "cfg5_multiturn_mix_70b": cfg5_multiturn_mix_70b,
+WORKLOADS = {
+    "decode_8b_system_prompts": decode_8b_system_prompts,
+    "fewshot_extend": fewshot_extend,
+    "forked_decode_70b": forked_decode_70b,
+    "multiturn_mix_70b": multiturn_mix_70b,
 }
