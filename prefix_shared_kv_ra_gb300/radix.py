@@ -98,6 +98,11 @@ class RadixCache:
         self.evictable_size = 0  # tokens in nodes no running request references (all can be evicted)
 
     # ------------------------------------------------------------------ queries
+    def _child_key(self, key: np.ndarray):
+        """A child is found by the first page of its edge: siblings may share leading tokens within
+        a page (an edge is split on page boundaries only), never a whole first page."""
+        return int(key[0]) if self.page == 1 else tuple(key[:self.page].tolist())
+
     def _tick(self) -> int:
         self._clock += 1
         return self._clock
@@ -110,7 +115,7 @@ class RadixCache:
         now = self._tick()
         node.last_access = now
         while pos < key.size:
-            child = node.children.get(int(key[pos]))
+            child = node.children.get(self._child_key(key[pos:]))
             if child is None:
                 break
             k = _common_len(child.key, key[pos:]) // self.page * self.page
@@ -135,10 +140,10 @@ class RadixCache:
         mid = _Node(child.key[:k].copy(), child.value[:k].copy(), parent)
         mid.lock_ref = child.lock_ref
         mid.last_access = child.last_access
-        parent.children[int(mid.key[0])] = mid
+        parent.children[self._child_key(mid.key)] = mid
         child.key, child.value = child.key[k:].copy(), child.value[k:].copy()
         child.parent = mid
-        mid.children[int(child.key[0])] = child
+        mid.children[self._child_key(child.key)] = child
         return mid
 
     def insert(self, tokens: Sequence[int], slots: Sequence[int]) -> int:
@@ -154,7 +159,7 @@ class RadixCache:
         if k < key.size:
             leaf = _Node(key[k:].copy(), val[k:].copy(), node)
             leaf.last_access = self._tick()
-            node.children[int(leaf.key[0])] = leaf
+            node.children[self._child_key(leaf.key)] = leaf
             self.evictable_size += leaf.key.size
         return k
 
@@ -205,7 +210,7 @@ class RadixCache:
             freed += leaf.value.size
             self.evictable_size -= leaf.key.size
             parent = leaf.parent
-            del parent.children[int(leaf.key[0])]
+            del parent.children[self._child_key(leaf.key)]
             if parent is not self.root and not parent.children and parent.lock_ref == 0:
                 heapq.heappush(heap, (parent.last_access, parent.uid, parent))
         return freed

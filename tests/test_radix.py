@@ -234,3 +234,128 @@ def test_multilevel_short_nodes_fold_into_the_groups_below():
               for g, (s, e, l) in enumerate(zip(start, end, level))}
     # the 3-token node shared by rows 0-2 is too short: its positions join the node below (rows 0, 1)
     assert groups == {(0, 6, 0): [0, 1]} and nl == 1
+
+
+
+def _tree_pages(cache):
+    """Every cached page as (tokens from the root to the end of the page) -> (its slots), read from
+    the nodes.  With pages of one token this is every cached position and its slot."""
+    out, stack, P = {}, [(cache.root, ())], cache.page
+    while stack:
+        node, pre = stack.pop()
+        for c in node.children.values():
+            key, val = c.key.tolist(), c.value.tolist()
+            assert len(key) % P == 0 and len(key) > 0
+            p = pre
+            for j in range(0, len(key), P):
+                p = p + tuple(key[j:j + P])
+                out[p] = tuple(val[j:j + P])
+            stack.append((c, p))
+    return out
+
+
+@pytest.mark.parametrize("page", [1, 4])
+def test_random_operations_against_a_page_set_model(page):
+    """Seeded random requests, finishes and evictions against a plain model of the cache: the set of
+    cached pages, each named by the tokens from the root to its end (prefix-closed) and holding its
+    slots.  Two requests that differ inside a page own a page each.  A request matches its longest
+    cached run of whole pages, locks it, evicts if the pool is short, inserts its whole pages and
+    holds them until it finishes.  Checked after every operation: the match and the slots it returns,
+    the tree's pages and slots against the model, eviction only of unlocked pages (the least
+    recently used unlocked leaf first, everything left locked when it frees too little), slots freed
+    back to the pool exactly once, and the evictable-token count."""
+    rng = np.random.default_rng(7 + page)
+    pool = SlotPool(96, page_size=page)
+    cache = RadixCache(pool)
+    model = {}        # page path -> slots of the page
+    live = []         # (cached tokens of a running request, its locked node)
+    seen = []         # earlier requests, to fork from
+
+    def locked_pages():
+        return {tuple(toks[:j + page]) for toks, _ in live for j in range(0, len(toks), page)}
+
+    def check_state():
+        assert _tree_pages(cache) == model
+        assert cache.total_tokens() == page * len(model)
+        assert cache.evictable_size == page * (len(model) - len(locked_pages()))
+        slots = np.asarray(sorted(s for v in model.values() for s in v), dtype=np.int64)
+        assert np.unique(slots).size == slots.size                    # one token per slot
+        free_pages = set(pool._free)
+        assert not any(s // page in free_pages for s in slots.tolist())  # none on a free page
+        assert slots.size == 0 or slots.min() >= page                 # never the reserved page 0
+        assert pool.available() + slots.size == pool.num_slots - page  # nothing leaks
+        for p in model:                                               # prefix-closed
+            assert len(p) == page or p[:-page] in model
+
+    def evict(want):
+        before = _tree_pages(cache)
+        freed = cache.evict(want)
+        after = _tree_pages(cache)
+        removed = set(before) - set(after)
+        assert set(after) <= set(before) and all(after[p] == before[p] for p in after)
+        assert freed == page * len(removed)
+        assert not (removed & locked_pages())
+        for p in removed:
+            del model[p]
+        return freed, removed, after
+
+    for step in range(2500):
+        op = rng.random()
+        if op < 0.55:                                                  # a new request
+            if seen and rng.random() < 0.7:
+                base = seen[int(rng.integers(len(seen)))]
+                base = base[:int(rng.integers(0, len(base) + 1))]
+            else:
+                base = []
+            toks = base + rng.integers(0, 3, size=int(rng.integers(1, 10))).tolist()
+            got, node = cache.match_prefix(toks)
+            L = 0
+            while L + page <= len(toks) and tuple(toks[:L + page]) in model:
+                L += page
+            assert got.tolist() == [s for j in range(0, L, page) for s in model[tuple(toks[:j + page])]]
+            cache.lock(node)                                           # protect the hit while evicting
+            need = len(toks) - L
+            short = -(-need // page) * page - pool.available()
+            if short > 0:
+                evict(short)
+            new = pool.alloc(need)
+            if new is None:                  # everything left is locked: by running requests or this hit
+                assert set(model) == locked_pages() | {tuple(toks[:j + page]) for j in range(0, L, page)}
+                cache.unlock(node)
+                check_state()
+                continue
+            slots = np.concatenate([got, new]).astype(np.int32)
+            assert cache.insert(toks, slots) == L
+            n = len(toks) // page * page
+            if n < len(toks):
+                pool.free(slots[n:])                                   # the partial last page is the caller's
+            for j in range(L, n, page):
+                model[tuple(toks[:j + page])] = tuple(int(x) for x in slots[j:j + page])
+            cache.unlock(node)
+            if n > 0:
+                live.append((toks[:n], cache.path(toks[:n])[-1]))
+                cache.lock(live[-1][1])
+            seen.append(toks)
+        elif op < 0.85 and live:                                       # a request finishes
+            _, node = live.pop(int(rng.integers(len(live))))
+            cache.unlock(node)
+        else:                                                          # the scheduler evicts
+            want = int(rng.integers(1, 40))
+            leaves = [n for n in cache._leaves() if n.lock_ref == 0]
+            oldest_key = None
+            if leaves:
+                n = min(leaves, key=lambda x: (x.last_access, x.uid))
+                path = []
+                while n is not cache.root:
+                    path = n.key.tolist() + path
+                    n = n.parent
+                oldest_key = tuple(path)
+            avail = pool.available()
+            freed, removed, after = evict(want)
+            assert pool.available() == avail + freed
+            if freed < want:
+                assert len(after) == len(locked_pages())               # only locked pages are left
+            if freed > 0:
+                assert oldest_key in removed                          # least recently used leaf first
+        check_state()
+    assert len(seen) > 500
