@@ -359,3 +359,88 @@ def test_random_operations_against_a_page_set_model(page):
                 assert oldest_key in removed                          # least recently used leaf first
         check_state()
     assert len(seen) > 500
+
+
+def _random_tree_rows(rng, n):
+    """Slot rows of n requests with radix sharing: each row copies a prefix of an earlier row (or
+    nothing) and continues with fresh slots, so equal slots at a position mean an equal prefix."""
+    rows, fresh = [], iter(range(1000, 10 ** 6))
+    for _ in range(n):
+        row = []
+        if rows and rng.random() < 0.8:
+            parent = rows[int(rng.integers(len(rows)))]
+            row = parent[:int(rng.integers(0, len(parent) + 1))]
+        row = row + [next(fresh) for _ in range(int(rng.integers(1, 6)))]
+        rows.append(row)
+    return rows
+
+
+def _brute_force_shared_nodes(rows):
+    """The multi-level groups with min_range 1, from their definition by enumeration: every prefix p
+    of the rows cut one token short that at least two requests hold, and at which those requests do
+    not all continue with one same slot, ends a node; its group covers [end of the nearest such
+    prefix above it, len(p)) and its level counts those above it."""
+    seqs = [tuple(r[:len(r) - 1]) for r in rows]
+    members = {}
+    for b, s in enumerate(seqs):
+        for d in range(1, len(s) + 1):
+            members.setdefault(s[:d], set()).add(b)
+    ends = set()
+    for p, m in members.items():
+        if len(m) < 2:
+            continue
+        nxt = {seqs[b][len(p)] if len(seqs[b]) > len(p) else None for b in m}
+        if len(nxt) > 1 or None in nxt:
+            ends.add(p)
+    out = set()
+    for p in ends:
+        above = [len(q) for q in ends if len(q) < len(p) and p[:len(q)] == q]
+        out.add((max(above, default=0), len(p), len(above), tuple(sorted(members[p]))))
+    return out
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_multilevel_groups_against_brute_force(seed):
+    from prefix_shared_kv_ra_gb300.radix import cascade_groups_multilevel
+    rng = np.random.default_rng(300 + seed)
+    rows = _random_tree_rows(rng, int(rng.integers(2, 14)))
+    indptr, reqs, start, end, level, nl = cascade_groups_multilevel(rows)
+    got = {(int(start[g]), int(end[g]), int(level[g]), tuple(sorted(reqs[indptr[g]:indptr[g + 1]].tolist())))
+           for g in range(len(start))}
+    want = _brute_force_shared_nodes(rows)
+    assert got == want
+    assert nl == (1 + max(l for _, _, l, _ in want) if want else 0)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_group_builders_hold_their_invariants_on_random_trees(seed):
+    """Any min_range: each request's groups tile 0 .. (deepest end) - 1 one level after another, the
+    members of a group hold the same slots over its range, and the newest token stays private.  The
+    one-level builder: a group's prefix is shared by all its members and is maximal (it stops where
+    the shortest member's newest token begins, or where two members differ)."""
+    from prefix_shared_kv_ra_gb300.radix import cascade_groups_multilevel
+    rng = np.random.default_rng(500 + seed)
+    rows = _random_tree_rows(rng, int(rng.integers(2, 16)))
+    min_range = int(rng.integers(1, 6))
+    indptr, reqs, start, end, level, nl = cascade_groups_multilevel(rows, min_range=min_range)
+    cover = {}
+    for g in range(len(start)):
+        mem = reqs[indptr[g]:indptr[g + 1]].tolist()
+        assert len(mem) >= 2 and end[g] > start[g]
+        for m in mem:
+            assert rows[m][start[g]:end[g]] == rows[mem[0]][start[g]:end[g]]
+            cover.setdefault(m, []).append((int(start[g]), int(end[g]), int(level[g])))
+    for m, rng_ in cover.items():
+        rng_.sort()
+        assert [l for _, _, l in rng_] == list(range(len(rng_)))
+        assert rng_[0][0] == 0 and all(rng_[i][1] == rng_[i + 1][0] for i in range(len(rng_) - 1))
+        assert rng_[-1][1] <= len(rows[m]) - 1
+    gi, gr, gp = cascade_groups(rows)
+    for g in range(gi.size - 1):
+        mem = gr[gi[g]:gi[g + 1]].tolist()
+        assert len(mem) >= 2 and gp[g] >= 1
+        for m in mem:
+            assert rows[m][:gp[g]] == rows[mem[0]][:gp[g]] and gp[g] <= len(rows[m]) - 1
+        at_end = gp[g] == min(len(rows[m]) - 1 for m in mem)
+        differ = len({rows[m][gp[g]] for m in mem if len(rows[m]) > gp[g]}) > 1
+        assert at_end or differ
