@@ -73,3 +73,53 @@ def test_bf16_rounding_is_nearest_even():
     x = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5, 65504.0], np.float32)
     b = W.f32_to_bf16_bits(x)
     np.testing.assert_array_equal(W.bf16_bits_to_f32(b), [1.0, 1.0, 1.0 + 2 ** -6, -2.5, 65536.0])
+
+
+def _check_new_tokens_and_sharing(b):
+    """The step's new tokens sit where the calls read them, and the rows are radix-consistent."""
+    loc = b.out_cache_loc
+    n_ext = int(b.ext_extend_lens.sum())
+    assert loc.size == n_ext + b.n_decode
+    for i, (r, P, E) in enumerate(zip(b.ext_rpi, b.ext_prefix_lens, b.ext_extend_lens)):
+        q0, q1 = b.ext_qo_indptr[i], b.ext_qo_indptr[i + 1]
+        assert q1 - q0 == E
+        np.testing.assert_array_equal(b.req_to_token[r, P:P + E], loc[q0:q1])   # suffix after the prefix
+        assert not set(b.req_to_token[r, :P].tolist()) & set(loc.tolist())      # the prefix is cached
+    for j, (r, L) in enumerate(zip(b.dec_rpi, b.dec_seq_lens)):
+        assert b.req_to_token[r, L - 1] == loc[n_ext + j]                        # the new token is last
+        assert not set(b.req_to_token[r, :L - 1].tolist()) & set(loc.tolist())
+    rows = [b.req_to_token[r, :L] for r, L in
+            list(zip(b.ext_rpi, b.ext_prefix_lens + b.ext_extend_lens)) + list(zip(b.dec_rpi, b.dec_seq_lens))]
+    # a slot is one position of one prefix: every slot has one (position, preceding slot) pair, so by
+    # induction over the positions every row that holds it agrees on everything before it
+    slot = np.concatenate(rows).astype(np.int64)
+    pos = np.concatenate([np.arange(r.size) for r in rows])
+    pred = np.concatenate([np.r_[-1, r[:-1]] for r in rows]).astype(np.int64)
+    pairs = np.unique(np.stack([slot, pos, pred], axis=1), axis=0)
+    assert np.unique(pairs[:, 0]).size == pairs.shape[0]
+    if b.has_cascade():
+        starts = b.casc_group_start if b.casc_group_start is not None else \
+            np.zeros(b.casc_group_indptr.size - 1, np.int32)
+        for g in range(b.casc_group_indptr.size - 1):
+            mem = b.casc_group_reqs[b.casc_group_indptr[g]:b.casc_group_indptr[g + 1]]
+            s, e = int(starts[g]), int(b.casc_group_prefix_len[g])
+            assert len(mem) >= 2 and 0 <= s < e
+            for m in mem:
+                assert e <= b.dec_seq_lens[m] - 1                                 # the new token stays private
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_mixed_new_tokens_and_sharing(seed):
+    rng = np.random.default_rng(seed)
+    hkv = int(rng.choice([1, 2, 4, 8]))
+    b = W.random_mixed(100 + seed, n_extend=int(rng.integers(0, 6)), n_decode=int(rng.integers(1, 9)),
+                       num_q_heads=hkv * int(rng.choice([1, 2, 4])), num_kv_heads=hkv, head_dim=64,
+                       max_len=int(rng.choice([20, 130, 400])), share_prob=float(rng.uniform(0, 0.95)),
+                       with_cascade=bool(seed % 2), page_size=int(rng.choice([1, 1, 4])))
+    _check_batch(b)
+    _check_new_tokens_and_sharing(b)
+
+
+@pytest.mark.parametrize("name", ["decode_8b_system_prompts", "fewshot_extend", "forked_decode_70b"])
+def test_workload_new_tokens_and_sharing(name):
+    _check_new_tokens_and_sharing(W.WORKLOADS[name]())
