@@ -34,36 +34,54 @@ __all__ = ["SlotPool", "RadixCache", "cascade_groups"]
 
 class SlotPool:
     """Free list of token slots in pages of `page_size` consecutive slots; page 0 (holding slot 0,
-    the dummy slot padded requests write) is never handed out."""
+    the dummy slot padded requests write) is never handed out.  The free pages form a stack: the
+    lowest pages go out first at the start, and freed pages are handed out again before older ones.
+    Freeing a page that is already free raises (it would be handed out twice)."""
 
     def __init__(self, num_slots: int, page_size: int = 1):
         if page_size < 1 or num_slots % page_size:
             raise ValueError("num_slots must be a multiple of page_size")
         self.num_slots = int(num_slots)
         self.page_size = int(page_size)
-        self._free = list(range(self.num_slots // page_size - 1, 0, -1))  # free pages; pop() gives low ones first
+        n_pages = self.num_slots // page_size
+        self._stack = np.arange(n_pages - 1, 0, -1, dtype=np.int64)  # free pages; the top is handed out first
+        self._top = self._stack.size
+        self._is_free = np.ones(n_pages, dtype=bool)
+        self._is_free[0] = False
 
     def available(self) -> int:
         """Free slots (whole pages)."""
-        return len(self._free) * self.page_size
+        return self._top * self.page_size
+
+    def free_pages(self) -> np.ndarray:
+        """The free pages, the next one to be handed out last."""
+        return self._stack[:self._top].copy()
 
     def alloc(self, n: int) -> Optional[np.ndarray]:
         """Slots for n new tokens, in order: the first n slots of ceil(n / page_size) fresh pages (the rest
         of the last page stays with the caller until freed)."""
         pages = -(-n // self.page_size)
-        if pages > len(self._free):
+        if pages > self._top:
             return None
-        out = np.asarray([self._free.pop() for _ in range(pages)], dtype=np.int64)
+        out = self._stack[self._top - pages:self._top][::-1].copy()
+        self._top -= pages
+        self._is_free[out] = False
         slots = (out[:, None] * self.page_size + np.arange(self.page_size)[None, :]).reshape(-1)[:n]
         return slots.astype(np.int32)
 
     def free(self, slots: Sequence[int]) -> None:
         """Return the pages holding these slots."""
         s = np.asarray(slots, dtype=np.int64)
-        if s.size and (s.min() < self.page_size or s.max() >= self.num_slots):
+        if s.size == 0:
+            return
+        if s.min() < self.page_size or s.max() >= self.num_slots:
             raise ValueError("slot out of range")
-        for pg in np.unique(s // self.page_size).tolist():
-            self._free.append(int(pg))
+        pages = np.unique(s // self.page_size)
+        if self._is_free[pages].any():
+            raise ValueError("a page freed twice")
+        self._stack[self._top:self._top + pages.size] = pages
+        self._top += pages.size
+        self._is_free[pages] = True
 
 
 class _Node:

@@ -280,7 +280,7 @@ def test_random_operations_against_a_page_set_model(page):
         assert cache.evictable_size == page * (len(model) - len(locked_pages()))
         slots = np.asarray(sorted(s for v in model.values() for s in v), dtype=np.int64)
         assert np.unique(slots).size == slots.size                    # one token per slot
-        free_pages = set(pool._free)
+        free_pages = set(pool.free_pages().tolist())
         assert not any(s // page in free_pages for s in slots.tolist())  # none on a free page
         assert slots.size == 0 or slots.min() >= page                 # never the reserved page 0
         assert pool.available() + slots.size == pool.num_slots - page  # nothing leaks
@@ -444,3 +444,37 @@ def test_group_builders_hold_their_invariants_on_random_trees(seed):
         at_end = gp[g] == min(len(rows[m]) - 1 for m in mem)
         differ = len({rows[m][gp[g]] for m in mem if len(rows[m]) > gp[g]}) > 1
         assert at_end or differ
+
+
+@pytest.mark.parametrize("page", [1, 4, 16])
+def test_slot_pool_against_a_list_model(page):
+    """The pool hands out exactly the slots a plain list of free pages would (pop the last; a free
+    appends the pages in increasing order), keeps count, and refuses a page freed twice."""
+    rng = np.random.default_rng(40 + page)
+    pool = SlotPool(64 * page, page_size=page)
+    model = list(range(63, 0, -1))
+    held = []
+    for _ in range(3000):
+        if held and rng.random() < 0.45:
+            slots = held.pop(int(rng.integers(len(held))))
+            pool.free(slots)
+            model.extend(np.unique(np.asarray(slots) // page).tolist())
+        else:
+            n = int(rng.integers(0, 5 * page))
+            got = pool.alloc(n)
+            pages = -(-n // page)
+            if pages > len(model):
+                assert got is None
+                continue
+            want = [model.pop() for _ in range(pages)]
+            assert got.tolist() == [pg * page + i for pg in want for i in range(page)][:n]
+            if n:
+                held.append(got)
+        assert pool.available() == len(model) * page
+        assert sorted(pool.free_pages().tolist()) == sorted(model)
+    if held:
+        pool.free(held[0])
+        with pytest.raises(ValueError):
+            pool.free(held[0])                                         # the same pages again
+    with pytest.raises(ValueError):
+        pool.free([0])                                                 # the reserved page
