@@ -102,8 +102,9 @@ def _common_len(a: np.ndarray, b: np.ndarray) -> int:
     n = min(a.size, b.size)
     if n == 0:
         return 0
-    diff = np.nonzero(a[:n] != b[:n])[0]
-    return int(diff[0]) if diff.size else n
+    neq = a[:n] != b[:n]
+    i = int(neq.argmax())  # the first mismatch (argmax of a boolean array stops at the first True)
+    return i if neq[i] else n
 
 
 class RadixCache:
@@ -149,8 +150,8 @@ class RadixCache:
             slots.append(child.value)
             node = child
             pos += k
-        value = np.concatenate(slots) if slots else np.zeros(0, np.int32)
-        return value.astype(np.int32), node
+        value = np.concatenate(slots) if slots else np.zeros(0, np.int32)  # a fresh array either way
+        return value.astype(np.int32, copy=False), node
 
     def _split(self, child: _Node, k: int) -> _Node:
         """Make the first k tokens of child's edge a new node between child and its parent."""
