@@ -38,6 +38,7 @@ WORKLOAD = ("multi-turn chat mix, 70B heads (64 q / 8 kv, head_dim 128, bf16): 2
             "contexts (median 2048, clipped 16..32768), radix-tree prefix sharing at 70% token hit ratio; "
             "32 extend (suffix 64..512) + 224 decode (cascade groups from the radix tree); pool 2M slots")
 L2_FLUSH_BYTES = 256 << 20
+NOMINAL_HBM_GBS = 8000.0  # the ~8 TB/s the problem statement quotes for GB300's HBM3e (context beside the measured peak)
 KV_BYTES_PER_TOKEN_HEAD = 2 * 128 * 2  # K + V row of one kv head, bf16
 
 
@@ -93,20 +94,24 @@ def source_digest() -> str:
 
 
 def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from profiles/ncu_traffic.md (lines 'traffic: kernel=.. workload=.. bytes=..
-    source=..'), or None when absent or taken on other sources."""
-    path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) recorded from an ncu capture in
+    profiles/traffic.json, or None when absent or captured on other sources (the record names the source
+    digest it was taken on).  A recorded figure, not one measured by this run: the line says so."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
-    digest = source_digest()
-    for line in open(path):
-        line = line.strip().strip("`")
-        if not line.startswith("traffic:"):
-            continue
-        kv = dict(x.split("=", 1) for x in line[len("traffic:"):].split())
-        if kv.get("kernel") == kernel and kv.get("workload") == workload and kv.get("source") == digest:
-            return float(kv["bytes"])
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("source_digest") != source_digest():
+        return None
+    for e in rec.get("launches", []):
+        if e.get("kernel") == kernel and e.get("workload") == workload:
+            return float(e["dram_bytes"])
     return None
+
+
+TRAFFIC_NOTE = ("recorded, not measured by this run: DRAM bytes per launch from a one-pass ncu capture of the same "
+                "workload (profiles/traffic.json), used only while its source digest equals this build's")
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -365,7 +370,7 @@ def e2e_steps(step, steps: int, warmup: int, flush):
     return ms, h2d, d2h, same
 
 
-def extra_kernels(dev, flush, peaks, reps: int = 20):
+def extra_kernels(dev, flush, peaks, reps: int = 20, with_oracle: bool = True):
     """The same kernels on the other workloads (parity-tested elsewhere): per-kernel roofline."""
     import workloads as W
     out = {}
@@ -392,9 +397,17 @@ def extra_kernels(dev, flush, peaks, reps: int = 20):
                 out[key] = {"kernel": "decode" + (" + cascade prefix pass" if casc else ""), "ms": ms,
                             "tokens_per_s": b.n_decode / ms * 1e3, "algorithmic_bytes": db["algorithmic"],
                             "gbs": gbs, "frac_of_measured_hbm": gbs / peaks["hbm_gbs"],
+                            "frac_of_nominal_8tbs": gbs / NOMINAL_HBM_GBS,
                             "effective_gbs": db["logical"] / ms / 1e6}
             out[key]["device_error"] = r["device_error"]
             del st
+        if with_oracle and not name.endswith("_page16"):
+            # the oracle on the same batch, the whole call's rows, timed on the host cores
+            o = oracle_step(b)
+            for casc in modes:
+                out[name + ("_cascade" if casc else "")]["oracle"] = {
+                    "tokens_per_s": o["tokens_per_s"], "seconds": o["seconds"], "cores": o["cores"],
+                    "rows": o["rows"], "kind": "fp64 oracle, every query row of the call, measured"}
     # the decode step's store fused into the decode call, against the two calls (whole steps, no events
     # between the calls, so the programmatic launch chain is kept in both)
     b = W.decode_8b_system_prompts()
@@ -412,6 +425,7 @@ def extra_kernels(dev, flush, peaks, reps: int = 20):
         "separate_store_then_decode_ms": steps[False][0], "tokens_per_s": b.n_decode / ms * 1e3,
         "algorithmic_bytes": nbytes, "gbs": nbytes / ms / 1e6,
         "frac_of_measured_hbm": nbytes / ms / 1e6 / peaks["hbm_gbs"],
+        "frac_of_nominal_8tbs": nbytes / ms / 1e6 / NOMINAL_HBM_GBS,
         "device_error": steps[True][1] | steps[False][1]}
     return out
 
@@ -435,60 +449,67 @@ def serving_replay(dev, convs: int = 192, turns: int = 4):
 
 
 # ----------------------------------------------------------------------------- CPU oracle arm
-def oracle_sample(b, budget_s: float, seed: int = 0):
-    """Time the fp64 oracle on a random sample of the step's query rows, about `budget_s`
-    seconds of work, and extrapolate to the whole step by key visits."""
+def bench_config(b, world: int = 1) -> dict:
+    """The `config` of the bench line: the same dict for the GPU arm and the oracle (reference) arm."""
+    return {"workload": WORKLOAD, "global_batch": 256 * world, "replica_extend_tokens": b.total_q_extend,
+            "replica_decode_tokens": b.n_decode,
+            "l2": "GPU: flushed by a 256 MB write between steps; oracle: its 8 GiB pool exceeds every CPU cache",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "hit_ratio": round(b.meta["construction_hit_ratio"], 4)}
+
+
+def oracle_step(b, pool=None, fraction: float = 1.0) -> dict:
+    """One step of the fp64 oracle on the host cores, timed: every extend and decode query row of the batch
+    (or, with fraction < 1, every round(1/fraction)-th (token, head) row of each part).  tokens = rows / Hq."""
     import oracle
-    rng = np.random.default_rng(seed)
-    pool = oracle.pool_after_store(b)
+    pool = pool or oracle.pool_after_store(b)
     hq = b.num_q_heads
-    # key visits per query row
-    ext_keys = np.repeat(np.concatenate([b.ext_prefix_lens[i] + 1 + np.arange(b.ext_extend_lens[i])
-                                         for i in range(b.n_extend)]) if b.n_extend else np.zeros(0), hq)
-    dec_keys = np.repeat(b.dec_seq_lens.astype(np.float64), hq)
-    total_visits = float(ext_keys.sum() + dec_keys.sum())
-    threads = oracle.num_threads()
+    n_e, n_d = b.total_q_extend * hq, b.n_decode * hq
+    stride = max(1, int(round(1.0 / fraction))) if fraction < 1.0 else 1
+    se = None if stride == 1 else np.arange(0, n_e, stride, dtype=np.int64)
+    sd = None if stride == 1 else np.arange(0, n_d, stride, dtype=np.int64)
+    t0 = time.perf_counter()
+    if n_e:
+        oracle.extend_batch(b, sel=se, pool=pool)
+    if n_d:
+        oracle.decode_batch(b, sel=sd, pool=pool)
+    dt = time.perf_counter() - t0
+    rows = (n_e if se is None else se.size) + (n_d if sd is None else sd.size)
+    return {"seconds": dt, "tokens": rows / hq, "tokens_per_s": rows / hq / dt, "cores": oracle.num_threads(),
+            "rows": int(rows), "all_rows": stride == 1}
 
-    def timed(n_e, n_d):
-        se = np.sort(rng.choice(ext_keys.size, size=min(n_e, ext_keys.size), replace=False)) if ext_keys.size else None
-        sd = np.sort(rng.choice(dec_keys.size, size=min(n_d, dec_keys.size), replace=False)) if dec_keys.size else None
-        t0 = time.perf_counter()
-        if se is not None:
-            oracle.extend_batch(b, sel=se, pool=pool)
-        if sd is not None:
-            oracle.decode_batch(b, sel=sd, pool=pool)
-        v = (ext_keys[se].sum() if se is not None else 0) + (dec_keys[sd].sum() if sd is not None else 0)
-        return time.perf_counter() - t0, float(v)
 
-    # calibrate on small samples (the first also pays one-time start-up), then time one sample sized to
-    # about budget_s
-    timed(16, 16)
-    dt, v = timed(64, 64)
-    scale = max(1.0, budget_s / max(dt, 1e-3))
-    n_e = int(min(ext_keys.size, 64 * scale))
-    n_d = int(min(dec_keys.size, 64 * scale))
-    spent, visits = timed(n_e, n_d)
-    est_step_s = spent * total_visits / max(visits, 1.0)
-    tokens = b.total_q_extend + b.n_decode
-    return {"value": tokens / est_step_s, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{int(visits)} of {int(total_visits)} key visits ({100 * visits / total_visits:.2f}%) of "
-                      f"random query rows, {spent:.1f} s, extrapolated by key visits", "seconds": spent}
+def oracle_baseline(b, fraction: float = 1.0) -> dict:
+    """cpu_baseline of the GPU line: the oracle as it stands on one step of the same batch, measured."""
+    r = oracle_step(b, fraction=fraction)
+    what = ("the whole step" if r["all_rows"] else f"every {int(round(1 / fraction))}-th query row of the step")
+    return {"value": r["tokens_per_s"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+            "sample": f"{what}: {r['rows']} (token, q head) rows of extend and decode attention in fp64, "
+                      f"{r['seconds']:.1f} s on {r['cores']} host threads, no extrapolation",
+            "seconds": r["seconds"]}
 
 
 def run_reference(args):
+    """The reference arm: the fp64 oracle (the only implementation the pages allow to be written from
+    them) on the GPU arm's workload, one whole step per timed step on the host cores."""
     import workloads as W
-    b = W.multiturn_mix_70b()
-    res = [oracle_sample(b, args.ref_budget, seed=k) for k in range(args.warmup + args.steps)]
-    timed = res[args.warmup:]
-    val = float(np.mean([r["value"] for r in timed]))
-    tokens = b.total_q_extend + b.n_decode
+    import oracle
+    b = with_tree_groups(W.multiturn_mix_70b(seed=5))
+    pool = oracle.pool_after_store(b)
+    for _ in range(args.warmup):  # the CPU has nothing to warm beyond its first pass: short warm-up steps
+        oracle_step(b, pool, fraction=min(args.ref_fraction, 1.0 / 16))
+    timed = [oracle_step(b, pool, fraction=args.ref_fraction) for _ in range(args.steps)]
+    secs = float(np.mean([r["seconds"] for r in timed]))
+    val = timed[0]["tokens"] / secs
+    what = "whole step" if timed[0]["all_rows"] else f"every {int(round(1 / args.ref_fraction))}-th query row"
+    sample = (f"{what}: {timed[0]['rows']} (token, q head) rows per timed step, fp64, {timed[0]['cores']} host "
+              f"threads, {secs:.2f} s per step measured (warm-up steps: 1/16 of the rows)")
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tokens / val * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": 256, "tokens_per_step": tokens,
-                       "l2": "n/a (CPU)"},
+            "config": bench_config(b, args.gpus),
             "cpu_baseline": {"value": val, "unit": UNIT, "cores": timed[0]["cores"], "kind": "oracle",
-                             "sample": timed[0]["sample"]},
+                             "sample": sample},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -545,8 +566,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the per-kernel runs on the other workloads")
-    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds of oracle work per reference step")
+    ap.add_argument("--cpu-fraction", type=float, default=1.0,
+                    help="share of the step's query rows the cpu_baseline oracle runs (1 = the whole step)")
+    ap.add_argument("--ref-fraction", type=float, default=1.0,
+                    help="share of the step's query rows per reference (oracle) step (1 = the whole step)")
     ap.add_argument("--profile", default=None, choices=sorted(PROFILE_CASES),
                     help="untimed: run the hot path of one workload --steps times (for an ncu capture)")
     args = ap.parse_args()
@@ -618,31 +641,32 @@ def main():
         roof = {"kernel": "attn_tc_kernel<extend>", "bound": "tensor", "achieved": ext_tf,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ext_tf / peaks["bf16_tflops"],
                 "traffic": recorded_traffic("attn_tc_kernel<extend>", "multiturn_mix"),
+                "traffic_source": TRAFFIC_NOTE,
                 "peak_source": peaks["source"] + " bf16 burst",
                 "per_launch": {"flops": fl, "ms": ext_ms}}
     else:
         roof = {"kernel": "decode_kernel + decode_combine_kernel", "bound": "hbm", "achieved": dec_gbs,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
                 "traffic": recorded_traffic("decode_kernel", "multiturn_mix"),
+                "traffic_source": TRAFFIC_NOTE,
                 "peak_source": peaks["source"] + " HBM copy",
                 "per_launch": {"bytes": dbytes["algorithmic"], "ms": dec_ms}}
     extra = {} if args.no_extra else extra_kernels(dev, flush, peaks)
     replay = {} if args.no_extra else serving_replay(dev)
-    cpu = oracle_sample(b, args.cpu_budget)
+    cpu = oracle_baseline(b, args.cpu_fraction)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "global_batch": 256 * world, "tokens_per_step": job_tokens,
-                   "extend_tokens": b.total_q_extend, "decode_tokens": b.n_decode, "l2": "flushed (256 MB write)",
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "hit_ratio": round(b.meta["construction_hit_ratio"], 4)},
+        "config": bench_config(b, world),
+        "tokens_per_step": job_tokens,
         "roofline": roof,
         "kernels": {
             "step_breakdown_ms": {"kv_store": st_ms, "extend": ext_ms, "decode": dec_ms},
             "extend": {"tflops": ext_tf, "frac_of_measured_bf16": ext_tf / peaks["bf16_tflops"],
                        "flops": fl},
             "decode": {"gbs": dec_gbs, "frac_of_measured_hbm": dec_gbs / peaks["hbm_gbs"],
+                       "frac_of_nominal_8tbs": dec_gbs / NOMINAL_HBM_GBS,
                        "effective_gbs": dbytes["logical"] / dec_ms / 1e6, "unique_tokens": dbytes["unique_tokens"],
                        "logical_tokens": dbytes["logical_tokens"]},
             "kv_store": {"gbs": store_bytes(b) / st_ms / 1e6},

@@ -100,9 +100,6 @@ ra_status ra_kv_store(void* k_pool, void* v_pool, int64_t num_slots, int32_t num
  *   max_extend_len, max_prefix_len: host-side upper bounds of those arrays
  *                    (grid sizing); a device value above its bound is flagged
  *                    RA_DEVERR_LENGTH and the rows above the bound are skipped.
- * The suffix keys must already be stored (ra_kv_store) and listed in the table.
- * Rows with extend_lens[b] == 0 write nothing; prefix_lens[b] == 0 is plain
- * causal attention.  batch == 0 or total_q == 0 is a no-op.
  *   workspace:       device scratch of at least ra_extend_workspace_bytes(batch,
  *                    total_q, num_q_heads, num_kv_heads) bytes, 16-byte aligned
  *                    (may be NULL when batch or total_q is 0); it holds the
@@ -115,7 +112,9 @@ ra_status ra_kv_store(void* k_pool, void* v_pool, int64_t num_slots, int32_t num
  * Rows with extend_lens[b] == 0 write nothing; prefix_lens[b] == 0 is plain
  * causal attention.  batch == 0 or total_q == 0 is a no-op.  A request with
  * prefix_lens[b] + extend_lens[b] > table_stride is flagged RA_DEVERR_LENGTH and
- * skipped; the sum of extend_lens must not exceed total_q (excess tiles are
+ * skipped, and so is a request whose rows qo_indptr[b] .. qo_indptr[b] +
+ * extend_lens[b] - 1 do not lie inside [0, total_q): no row outside o is ever
+ * written.  The sum of extend_lens must not exceed total_q (excess tiles are
  * flagged RA_DEVERR_LENGTH and skipped).
  * Runs on tcgen05 tensor cores with TMEM accumulators; K/V rows are gathered
  * from the pool into 128B-swizzled shared-memory tiles, the query tile comes
@@ -233,7 +232,9 @@ ra_status ra_decode_attention_store(void* k_pool, void* v_pool, int64_t num_slot
  *   A call whose ra_decode_workspace_bytes(...) exceeds that size returns
  *   RA_ERR_WORKSPACE with a message and launches nothing.
  *   The first call on a device (with that device current) looks up the array's
- *   device address; make that first call outside any stream capture.
+ *   device address; the address is kept for that device's current CUDA context
+ *   and looked up again in a new context (after cudaDeviceReset, for
+ *   instance).  Make the first call in each context outside any stream capture.
  *   All calls share the array and it keeps the last call's contents: calls
  *   that overlap on the GPU (other streams, unordered threads) race on it.
  */

@@ -243,12 +243,15 @@ def ra_decode_attention_static(k_pool: torch.Tensor, v_pool: torch.Tensor, q: to
         raise ValueError("q/o shape mismatch")
     bf, i32 = torch.bfloat16, torch.int32
     ng = 0 if group_indptr is None else group_indptr.shape[0] - 1
-    _check(load().ra_decode_attention_static(
-        _ptr(k_pool, bf, "k_pool", dev), _ptr(v_pool, bf, "v_pool", dev), S, hkv, d, _ptr(q, bf, "q", dev),
-        _ptr(o, bf, "o", dev), hq, float(sm_scale), _ptr(req_to_token, i32, "req_to_token", dev),
-        req_to_token.shape[1], req_to_token.shape[0], _ptr(req_pool_indices, i32, "req_pool_indices", dev),
-        _ptr(seq_lens, i32, "seq_lens", dev), batch, int(max_seq_len), ng,
-        _ptr(group_indptr, i32, "group_indptr", dev), _ptr(group_reqs, i32, "group_reqs", dev),
-        _ptr(group_prefix_start, i32, "group_prefix_start", dev), _ptr(group_prefix_len, i32, "group_prefix_len", dev),
-        _ptr(group_level, i32, "group_level", dev), int(max_group_prefix_len), int(max_group_size),
-        int(max_group_levels), _ptr(device_error, i32, "device_error", dev), _stream(dev, stream)))
+    # the library resolves its static scratch on the CURRENT device: make it the tensors' device
+    with torch.cuda.device(dev):
+        _check(load().ra_decode_attention_static(
+            _ptr(k_pool, bf, "k_pool", dev), _ptr(v_pool, bf, "v_pool", dev), S, hkv, d, _ptr(q, bf, "q", dev),
+            _ptr(o, bf, "o", dev), hq, float(sm_scale), _ptr(req_to_token, i32, "req_to_token", dev),
+            req_to_token.shape[1], req_to_token.shape[0], _ptr(req_pool_indices, i32, "req_pool_indices", dev),
+            _ptr(seq_lens, i32, "seq_lens", dev), batch, int(max_seq_len), ng,
+            _ptr(group_indptr, i32, "group_indptr", dev), _ptr(group_reqs, i32, "group_reqs", dev),
+            _ptr(group_prefix_start, i32, "group_prefix_start", dev),
+            _ptr(group_prefix_len, i32, "group_prefix_len", dev), _ptr(group_level, i32, "group_level", dev),
+            int(max_group_prefix_len), int(max_group_size), int(max_group_levels),
+            _ptr(device_error, i32, "device_error", dev), _stream(dev, stream)))

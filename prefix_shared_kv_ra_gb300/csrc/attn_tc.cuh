@@ -68,6 +68,7 @@ struct TcParams {
   const int32_t* qo_indptr;
   int32_t max_extend_len;
   int32_t max_prefix_len;
+  int64_t total_q;  // rows of q and o: every written row index is checked against it
   __nv_bfloat16* o;
   const int32_t* work_count;  // number of (request, query tile) entries in work_items
   const int32_t* work_items;  // [2 * entries]: request, query tile; longest key range first
@@ -169,11 +170,18 @@ __device__ __forceinline__ bool tc_job(const TcParams& p, int32_t item, Job& j, 
       if (report && tile == 0 && j.kh == 0) flag_error(p.err, RA_DEVERR_TABLE);
       return false;
     }
+    // the request's rows qo_indptr[b] .. qo_indptr[b] + E - 1 must lie inside o: a request whose
+    // lengths disagree with total_q writes nothing (flagged once)
+    const int64_t q_first = __ldg(p.qo_indptr + b);
+    if (q_first < 0 || q_first + E > p.total_q) {
+      if (report && tile == 0 && j.kh == 0) flag_error(p.err, RA_DEVERR_LENGTH);
+      return false;
+    }
     j.n_valid = min(kTiles * T, E - tile * kTiles * T);
     j.causal0 = P + tile * kTiles * T;
     j.kbeg = 0;
     j.kend = j.causal0 + j.n_valid;
-    j.q_tok0 = static_cast<int64_t>(__ldg(p.qo_indptr + b)) + tile * kTiles * T;
+    j.q_tok0 = q_first + tile * kTiles * T;
   } else {
     const int x = rest % p.grid_x;
     const int g = rest / p.grid_x;

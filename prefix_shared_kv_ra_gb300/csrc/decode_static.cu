@@ -12,15 +12,23 @@
 //
 // Set-up: the first call on a device, with that device current, looks up the
 // array's device address with cudaGetSymbolAddress (the array's name in host
-// code is only a host-side stand-in) and caches it per device.  Make that first
-// call outside any stream capture.  The call allocates nothing: no cudaMalloc,
-// no cudaFree, no allocating library routine.  It then runs the normal decode
+// code is only a host-side stand-in) and caches it per device, together with
+// the CUDA context it belongs to.  The address is valid for that context's
+// lifetime: after the context is destroyed and another one is created on the
+// device (cudaDeviceReset, for instance), the module is loaded again and the
+// array may sit elsewhere, so the first call in the new context looks it up
+// again (so does the first call of a host thread that has not used CUDA
+// before).  Make the first call in each context outside any stream capture.
+// The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+// library routine.  It then runs the normal decode
 // path with the array as its workspace, so its results are those of
 // ra_decode_attention.  All calls share the one array and it keeps the last
 // call's contents (the decode path writes every partial before reading it and
 // clears the one field that must start at zero itself), so calls that overlap
 // on the GPU -- on different streams, or on one stream from several threads
 // without ordering -- race on it.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "api_common.h"
@@ -33,20 +41,43 @@ __device__ __align__(256) uint8_t g_decode_scratch[RA_DECODE_STATIC_SCRATCH_BYTE
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of g_decode_scratch on the current device (looked up once per device).
+// The driver's cuCtxGetCurrent, taken through the runtime (the library does not link libcuda).
+using CtxGetCurrent = CUresult (*)(CUcontext*);
+CtxGetCurrent ctx_get_current() {
+  static CtxGetCurrent fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrent>(ptr);
+  });
+  return fn;
+}
+
+// Device address of g_decode_scratch on the current device, looked up once per device and context.
 ra_status scratch_for_current_device(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(RA_ERR_CUDA, "device ordinal %d out of range", dev);
+  CtxGetCurrent get_ctx = ctx_get_current();
+  if (!get_ctx) return fail(RA_ERR_CUDA, "cuCtxGetCurrent is not available from the driver");
+  // null on a host thread that has not used CUDA yet: the lookup below makes the device's context current
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) ctx = nullptr;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  if (ctx == nullptr || g_scratch_addr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_decode_scratch);
     if (e != cudaSuccess || p == nullptr)
       return fail(RA_ERR_CUDA, "cudaGetSymbolAddress(static decode scratch): %s", cudaGetErrorString(e));
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return fail(RA_ERR_CUDA, "no current CUDA context");
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_addr[dev];
   return RA_OK;

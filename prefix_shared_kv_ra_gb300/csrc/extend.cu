@@ -362,6 +362,7 @@ extern "C" ra_status ra_extend_attention(const void* k_pool, const void* v_pool,
   p.qo_indptr = qo_indptr;
   p.max_extend_len = max_extend_len;
   p.max_prefix_len = max_prefix_len;
+  p.total_q = total_q;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.work_count = ws.count;
   p.work_counter = ws.counter;

@@ -5,6 +5,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
+import oracle
 import prefix_shared_kv_ra_gb300 as ra
 import workloads as W
 
@@ -113,6 +114,25 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str):
         raise AssertionError(f"{what}: {bad.sum()} of {bad.size} elements outside 1e-2 + 1e-2|ref| "
                              f"(max err {err.max():.3e}; first at {tuple(i)}: got {got[tuple(i)]}, "
                              f"ref {ref[tuple(i)]})")
+
+
+def check_store(db: DeviceBatch):
+    """Run the store and check the whole pool (K and V) bit for bit against the pool before the store with
+    the oracle's rows at out_cache_loc."""
+    b = db.b
+    before_k, before_v = db.k_pool.clone(), db.v_pool.clone()
+    db.store()
+    torch.cuda.synchronize()
+    assert int(db.err.item()) == 0
+    # the oracle's store over the slots it writes (rows relabelled 0..N-1: the store commutes with that)
+    loc = b.out_cache_loc.astype(np.int64)
+    idx = torch.from_numpy(loc).to(db.dev)
+    rows_k = before_k.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
+    rows_v = before_v.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
+    exp_k, exp_v = oracle.kv_store(rows_k, rows_v, b.k_new, b.v_new, np.arange(loc.size, dtype=np.int32))
+    for before, exp, got in ((before_k, exp_k, db.k_pool), (before_v, exp_v, db.v_pool)):
+        before.index_copy_(0, idx, torch.from_numpy(exp.view(np.int16)).to(db.dev).view(torch.bfloat16))
+        assert torch.equal(before.view(torch.int16), got.view(torch.int16))
 
 
 def attach_tree_groups(b: W.Batch, min_prefix: int = 256) -> W.Batch:

@@ -1,5 +1,6 @@
 """Host logic of bench.py (no GPU): the recorded DRAM traffic is used only for the sources it was
 taken on, and the clock record names this GPU's median SM clock and every throttle reason seen."""
+import json
 import os
 import shutil
 
@@ -16,37 +17,53 @@ def _tree(tmp_path):
     return root
 
 
+def _record(root, digest, launches):
+    (root / "profiles" / "traffic.json").write_text(json.dumps(
+        {"source_digest": digest, "command": "ncu ...", "launches": launches}))
+
+
 def test_recorded_traffic_follows_the_source_digest(tmp_path, monkeypatch):
     root = _tree(tmp_path)
     monkeypatch.setattr(bench, "ROOT", str(root))
     digest = bench.source_digest()
     assert digest != "" and len(digest) == 16
-    (root / "profiles" / "ncu_traffic.md").write_text(
-        "# traffic\n\n"
-        f"`traffic: kernel=attn_tc_kernel<extend> workload=multiturn_mix bytes=123456 source={digest}`\n"
-        "`traffic: kernel=decode_kernel workload=multiturn_mix bytes=999 source=0000000000000000`\n")
+    _record(root, digest, [{"kernel": "attn_tc_kernel<extend>", "workload": "multiturn_mix", "dram_bytes": 123456},
+                           {"kernel": "decode_kernel", "workload": "decode_8b", "dram_bytes": 999}])
     assert bench.recorded_traffic("attn_tc_kernel<extend>", "multiturn_mix") == 123456.0
     assert bench.recorded_traffic("attn_tc_kernel<extend>", "decode_8b") is None      # other workload
-    assert bench.recorded_traffic("decode_kernel", "multiturn_mix") is None           # other sources
+    assert bench.recorded_traffic("decode_kernel", "multiturn_mix") is None           # not recorded
+    # a record of other sources is not used
+    _record(root, "0000000000000000", [{"kernel": "decode_kernel", "workload": "multiturn_mix", "dram_bytes": 5}])
+    assert bench.recorded_traffic("decode_kernel", "multiturn_mix") is None
+    _record(root, digest, [{"kernel": "attn_tc_kernel<extend>", "workload": "multiturn_mix", "dram_bytes": 123456}])
     # any change to a kernel source (a comment included) retires the figure
     src = root / "prefix_shared_kv_ra_gb300" / "csrc" / "attn_tc.cuh"
     src.write_text(src.read_text() + "\n// edited\n")
     assert bench.source_digest() != digest
     assert bench.recorded_traffic("attn_tc_kernel<extend>", "multiturn_mix") is None
-    # no profile at all
-    (root / "profiles" / "ncu_traffic.md").unlink()
+    # no record at all
+    (root / "profiles" / "traffic.json").unlink()
     assert bench.recorded_traffic("attn_tc_kernel<extend>", "multiturn_mix") is None
 
 
-def test_committed_traffic_lines_parse():
-    """Every traffic line of the committed profile has kernel, workload, integer bytes and a digest."""
-    path = os.path.join(bench.ROOT, "profiles", "ncu_traffic.md")
-    lines = [ln.strip().strip("`") for ln in open(path) if ln.strip().strip("`").startswith("traffic:")]
-    assert lines
-    for ln in lines:
-        kv = dict(x.split("=", 1) for x in ln[len("traffic:"):].split())
-        assert set(kv) == {"kernel", "workload", "bytes", "source"}
-        assert int(kv["bytes"]) > 0 and len(kv["source"]) == 16
+def test_committed_traffic_record_is_complete():
+    """The committed record names its command, a 16-digit source digest and integer bytes per launch."""
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    assert "ncu" in rec["command"] and "--clock-control none" in rec["command"]
+    assert len(rec["source_digest"]) == 16
+    assert rec["launches"]
+    for e in rec["launches"]:
+        assert {"kernel", "workload", "dram_bytes"} <= set(e) and int(e["dram_bytes"]) > 0
+
+
+def test_both_arms_print_the_same_config():
+    """The GPU line and the oracle (reference) line describe the workload with one dict."""
+    class B:
+        total_q_extend, n_decode, meta = 9195, 224, {"construction_hit_ratio": 0.70091}
+    assert bench.bench_config(B(), 1) == bench.bench_config(B(), 1)
+    c = bench.bench_config(B(), 1)
+    assert c["parallelism"] == "single GPU" and c["global_batch"] == 256 and "l2" in c
 
 
 def test_clock_summary_picks_this_gpu_and_flags_reasons(tmp_path):

@@ -5,9 +5,9 @@ import numpy as np
 import pytest
 
 import workloads as W
-from helpers import DeviceBatch
+from helpers import DeviceBatch, check_store
 from test_gpu_extend import check_cascade, check_extend
-from test_gpu_store_decode import check_decode, check_store
+from test_gpu_store_decode import check_decode
 
 pytestmark = pytest.mark.gpu
 

@@ -17,28 +17,6 @@ def _pool_rows(t: torch.Tensor, slots: np.ndarray) -> np.ndarray:
     return t.index_select(0, idx).view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def check_store(db: DeviceBatch, n_other: int = 256):
-    b = db.b
-    db.store()
-    torch.cuda.synchronize()
-    assert int(db.err.item()) == 0
-    rng = np.random.default_rng(0)
-    untouched = np.setdiff1d(rng.integers(0, b.num_slots, size=n_other), b.out_cache_loc)
-    sample = np.concatenate([b.out_cache_loc.astype(np.int64), untouched])
-    # oracle store on the sampled slots (the store commutes with relabelling slots)
-    before_k = np.zeros((sample.size, b.num_kv_heads, b.head_dim), np.uint16)
-    before_v = np.zeros_like(before_k)
-    pos = {s: i for i, s in enumerate(b.pool_slots.tolist())}
-    for j, s in enumerate(sample.tolist()):
-        if s in pos:
-            before_k[j] = b.pool_k[pos[s]]
-            before_v[j] = b.pool_v[pos[s]]
-    local = np.arange(b.out_cache_loc.size, dtype=np.int32)
-    exp_k, exp_v = oracle.kv_store(before_k, before_v, b.k_new, b.v_new, local)
-    np.testing.assert_array_equal(_pool_rows(db.k_pool, sample), exp_k)
-    np.testing.assert_array_equal(_pool_rows(db.v_pool, sample), exp_v)
-
-
 def check_decode(db: DeviceBatch, sel=None, cascade=False):
     b = db.b
     db.decode(cascade=cascade)
@@ -63,12 +41,6 @@ def test_store_tiny_bit_exact():
         got_v = db.v_pool.view(torch.int16).cpu().numpy().view(np.uint16)
         np.testing.assert_array_equal(got_k, k_ref)   # the whole pool, bit for bit
         np.testing.assert_array_equal(got_v, v_ref)
-
-
-@pytest.mark.parametrize("name", ["decode_8b_system_prompts", "fewshot_extend", "forked_decode_70b",
-                                  "multiturn_mix_70b"])
-def test_store_full_workloads(name):
-    check_store(DeviceBatch(W.WORKLOADS[name]()))
 
 
 def test_store_empty_and_bad_slot_flag():
@@ -141,26 +113,6 @@ def test_decode_single_token_contexts():
     v = to_f64(db.v_new).reshape(5, 2, 128)
     got = to_f64(db.dec_o).reshape(5, 8, 128)
     np.testing.assert_array_equal(got, np.repeat(v, 4, axis=1))
-
-
-@pytest.mark.parametrize("name", ["decode_8b_system_prompts", "forked_decode_70b"])
-def test_decode_full_workloads(name):
-    b = W.WORKLOADS[name]()
-    db = DeviceBatch(b)
-    db.store()
-    check_decode(db)
-
-
-def test_decode_multiturn_mix_sampled():
-    b = W.multiturn_mix_70b()
-    db = DeviceBatch(b)
-    db.store()
-    rng = np.random.default_rng(1)
-    sel = np.sort(rng.choice(b.n_decode * b.num_q_heads, size=384, replace=False))
-    # always include the longest context
-    longest = int(np.argmax(b.dec_seq_lens))
-    sel = np.unique(np.concatenate([sel, longest * b.num_q_heads + np.arange(b.num_q_heads)]))
-    check_decode(db, sel=sel)
 
 
 def test_decode_bad_table_row_is_flagged_not_faulted():

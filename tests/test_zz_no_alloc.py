@@ -5,10 +5,12 @@ its split-KV scratch in the library's static device array instead of a caller
 workspace.
 
 Called here through the C ABI (ctypes) and compared with the workspace entry
-point, ra_decode_attention, on two calls in a row, within the tolerance the
-other parity tests use.  This file is collected last so that a stop-at-first-
-failure run has already run every other test; it also passes on its own in a
-fresh process (its first call performs the per-device set-up).
+point, ra_decode_attention, on two calls in a row.  Both run the same kernels on
+the same inputs, so the outputs must agree bit for bit (which also puts them
+within the 1e-2 + 1e-2 |ref| tolerance the other parity tests use).  This file
+is collected last so that a stop-at-first-failure run has already run every
+other test; it also passes on its own in a fresh process (its first call
+performs the per-device set-up).
 """
 import ctypes
 
@@ -46,10 +48,15 @@ def _static_call(db: DeviceBatch, cascade: bool, out: torch.Tensor) -> int:
         ptr(db.err), stream)
 
 
-def _reference(db: DeviceBatch, cascade: bool) -> np.ndarray:
+def _reference(db: DeviceBatch, cascade: bool) -> torch.Tensor:
     db.decode(cascade=cascade)  # the workspace entry point
     torch.cuda.synchronize()
-    return to_f64(db.dec_o)
+    return db.dec_o.clone()
+
+
+def _same_bits(got: torch.Tensor, ref: torch.Tensor, what: str):
+    assert_close(to_f64(got), to_f64(ref), what)
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), f"{what}: not bit-identical"
 
 
 def test_static_scratch_decode_matches_workspace_decode_on_two_calls():
@@ -67,13 +74,30 @@ def test_static_scratch_decode_matches_workspace_decode_on_two_calls():
         assert _static_call(db, casc, out) == 0, ra.load().ra_last_error_message()
         torch.cuda.synchronize()
         assert int(db.err.item()) == 0
-        assert_close(to_f64(out), ref, f"{db.b.name} static-scratch decode")
+        _same_bits(out, ref, f"{db.b.name} static-scratch decode")
     # and once more on the first case, after the second case overwrote the scratch
     db, casc = cases[0]
     out = torch.full_like(db.dec_o, float("nan"))
     assert _static_call(db, casc, out) == 0
     torch.cuda.synchronize()
-    assert_close(to_f64(out), refs[0], "static-scratch decode, repeated")
+    _same_bits(out, refs[0], "static-scratch decode, repeated")
+
+
+def test_static_scratch_decode_python_binding():
+    """The binding's ra_decode_attention_static (it makes the tensors' device current for the call)."""
+    b = W.decode_8b_system_prompts()
+    db = DeviceBatch(b)
+    db.store()
+    ref = _reference(db, True)
+    out = torch.full_like(db.dec_o, float("nan"))
+    ra.ra_decode_attention_static(db.k_pool, db.v_pool, db.dec_q, out, db.table, db.dec_rpi, db.dec_lens,
+                                  max_seq_len=b.max_seq_len, sm_scale=b.sm_scale, group_indptr=db.g_indptr,
+                                  group_reqs=db.g_reqs, group_prefix_len=db.g_plen,
+                                  max_group_prefix_len=int(b.casc_group_prefix_len.max()),
+                                  max_group_size=int(np.diff(b.casc_group_indptr).max()), device_error=db.err)
+    torch.cuda.synchronize()
+    assert int(db.err.item()) == 0
+    _same_bits(out, ref, "static-scratch decode through the binding")
 
 
 def test_static_scratch_decode_rejects_sizes_beyond_the_array():
