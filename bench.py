@@ -8,7 +8,7 @@ hit ratio; 32 extend requests + 224 decode requests; 2M-slot pool):
   ra_kv_store (this step's 9.4K new tokens)  ->  ra_extend_attention  ->
   ra_decode_attention.
 value = attention tokens (extend suffix tokens + decode tokens) per second
-with inputs resident in HBM; L2 is flushed (256 MB write) between steps.
+with inputs resident in HBM; L2 is flushed between steps (a 256 MB write, then a 256 MB read).
 Extra objects: per-kernel roofline (decode KV GB/s vs measured HBM copy
 bandwidth, extend TFLOP/s vs measured dense BF16), e2e through the public API
 with host buffers, the CPU oracle as baseline, SM clocks during the timed
@@ -38,6 +38,27 @@ WORKLOAD = ("multi-turn chat mix, 70B heads (64 q / 8 kv, head_dim 128, bf16): 2
             "contexts (median 2048, clipped 16..32768), radix-tree prefix sharing at 70% token hit ratio; "
             "32 extend (suffix 64..512) + 224 decode (cascade groups from the radix tree); pool 2M slots")
 L2_FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Between timed steps: write one 256 MB buffer (evicts every line the last step left in L2), then read
+    another (evicts the first buffer's dirty lines, so their write-back happens here and not inside the next
+    step's kernels).  The step then starts with an L2 that holds none of its data and nothing dirty, as an
+    ncu capture with cache control does; a write-only flush charged the decode call ~10 us of write-backs."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+        self.acc = torch.zeros(1, dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.acc.copy_(self.r.sum().view(1))
+# Before each timed step the stream runs a ~0.5 ms GPU delay (after the L2 flush, outside the timed region), so
+# the host has enqueued the whole step before its first kernel starts and the events time the GPU's work, not
+# the Python binding's launch latency (serving replays its decode step from a CUDA graph for the same reason).
+HOST_LEAD_CYCLES = 1_000_000
 NOMINAL_HBM_GBS = 8000.0  # the ~8 TB/s the problem statement quotes for GB300's HBM3e (context beside the measured peak)
 KV_BYTES_PER_TOKEN_HEAD = 2 * 128 * 2  # K + V row of one kv head, bf16
 
@@ -275,10 +296,12 @@ class Step:
 def time_steps(step, steps: int, warmup: int, flush, sample_clocks_uuid=None, breakdown: bool = True):
     """Headline pass: events around each whole step only (the kernels of a step may overlap through
     programmatic dependent launch).  Breakdown pass: events between the three calls as well (which
-    serialises them) for the per-kernel times the roofline uses."""
+    serialises them) for the per-kernel times the roofline uses.  Each step starts after the L2 flush and a
+    GPU delay that lets the host enqueue the whole step first (HOST_LEAD_CYCLES)."""
     torch = step.torch
     for _ in range(warmup):
-        flush.zero_()
+        flush()
+        torch.cuda._sleep(HOST_LEAD_CYCLES)
         step.run()
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
@@ -289,7 +312,8 @@ def time_steps(step, steps: int, warmup: int, flush, sample_clocks_uuid=None, br
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for k in range(steps):
-            flush.zero_()
+            flush()
+            torch.cuda._sleep(HOST_LEAD_CYCLES)
             step.run(events=[evs[k][0], None, None, evs[k][1]])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
@@ -301,7 +325,8 @@ def time_steps(step, steps: int, warmup: int, flush, sample_clocks_uuid=None, br
     if breakdown:
         evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
         for k in range(steps):
-            flush.zero_()
+            flush()
+            torch.cuda._sleep(HOST_LEAD_CYCLES)
             step.run(events=evb[k])
         torch.cuda.synchronize()
         per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evb])  # store, extend, decode
@@ -346,7 +371,7 @@ def e2e_steps(step, steps: int, warmup: int, flush):
             comp.wait_event(ev_in[k])
             if k >= 2:
                 comp.wait_event(ev_out[k - 2])  # step k-2's outputs are back on the host
-            flush.zero_()
+            flush()
             d = {name: (v.view(torch.bfloat16) if v.dtype == torch.int16 else v) for name, v in dev_in[i].items()}
             step.run(d=d, outs=dev_out[i])
             ev_comp[k].record(comp)
@@ -453,7 +478,8 @@ def bench_config(b, world: int = 1) -> dict:
     """The `config` of the bench line: the same dict for the GPU arm and the oracle (reference) arm."""
     return {"workload": WORKLOAD, "global_batch": 256 * world, "replica_extend_tokens": b.total_q_extend,
             "replica_decode_tokens": b.n_decode,
-            "l2": "GPU: flushed by a 256 MB write between steps; oracle: its 8 GiB pool exceeds every CPU cache",
+            "l2": "GPU: flushed between steps (256 MB write, then 256 MB read: no step data, no dirty lines); "
+                  "oracle: its 8 GiB pool exceeds every CPU cache",
             "parallelism": "replicas" if world > 1 else "single GPU",
             "hit_ratio": round(b.meta["construction_hit_ratio"], 4)}
 
@@ -606,7 +632,7 @@ def main():
     # grouped by the radix tree (one-level cascade groups over shared prefixes of >= 256 tokens)
     b = with_tree_groups(W.multiturn_mix_70b(seed=5 + rank))
     step = Step(b, dev, cascade=True)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
