@@ -254,9 +254,9 @@ class Step:
         self.ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
         self.ext_ws = torch.empty(max(ra.ra_extend_workspace_bytes(b.n_extend, b.total_q_extend, b.num_q_heads, hkv),
                                       256), dtype=torch.uint8, device=dev)
-        # kernel launches per step: store, [work-list plan, extend,] [[zeroing, key_start scatter,] decode
-        # plan, [prefix pass,] decode, combine]
-        self.launches = 1 + (2 if b.n_extend else 0) + ((3 + (3 if self.cascade else 0)) if b.n_decode else 0)
+        # kernel launches per step: store, [work-list plan, extend,] [[set-up, prefix pass,] decode plan, decode,
+        # combine]
+        self.launches = 1 + (2 if b.n_extend else 0) + ((3 + (2 if self.cascade else 0)) if b.n_decode else 0)
         if self.fused_store:
             self.launches -= 1
 

@@ -61,6 +61,7 @@ struct TcParams {
   int64_t table_rows;
   uint32_t* err;
   int32_t* work_counter;  // item claim counter, zero before the launch
+  int32_t* done_counter;  // cascade prefix pass: each CTA adds one once all its partials are written
   // extend
   const int32_t* rpi;
   const int32_t* prefix_lens;
@@ -86,8 +87,8 @@ struct TcParams {
   int32_t max_seq_len;
   int32_t cchunk;
   int32_t max_csplits;
-  float* casc_o;
-  float* casc_lse;
+  float* casc_o;    // [casc_slots, batch, hq, D]
+  float* casc_lse;  // [casc_slots, batch, hq]
 };
 
 namespace tc {
@@ -768,10 +769,11 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
           }
         }
       } else {
-        int32_t b = __ldg(p.group_reqs + jb.mem0 + (row_valid ? tok : 0));
-        const bool write = row_valid && b >= 0 && b < p.batch;
-        const int64_t ps =
-            ((static_cast<int64_t>(write ? b : 0) * p.hq + jb.kh * G + (r % G)) * p.casc_slots + jb.slot);
+        // fp32 partial rows, one per thread, at [slot][member][q head] (the G heads of a member contiguous),
+        // written in whole 32-byte sectors
+        const int32_t member = __ldg(p.group_reqs + jb.mem0 + (row_valid ? tok : 0));
+        const bool write = row_valid && member >= 0 && member < p.batch;
+        const int64_t ps = (static_cast<int64_t>(jb.slot) * p.batch + (write ? member : 0)) * p.hq + jb.kh * G + (r % G);
         float* dst = p.casc_o + ps * D;
         uint32_t oa[D / 32][32];
 #pragma unroll
@@ -782,11 +784,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         for (int c = 0; c < D / 32; ++c) {
           const uint32_t (&ov)[32] = oa[c];
           if (write) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              d4[e] = make_float4(__uint_as_float(ov[4 * e]) * inv_l, __uint_as_float(ov[4 * e + 1]) * inv_l,
-                                  __uint_as_float(ov[4 * e + 2]) * inv_l, __uint_as_float(ov[4 * e + 3]) * inv_l);
+            for (int e = 0; e < 4; ++e)  // whole 32-byte sectors
+              st_global_v8(dst + c * 32 + 8 * e, __uint_as_float(ov[8 * e]) * inv_l,
+                           __uint_as_float(ov[8 * e + 1]) * inv_l, __uint_as_float(ov[8 * e + 2]) * inv_l,
+                           __uint_as_float(ov[8 * e + 3]) * inv_l, __uint_as_float(ov[8 * e + 4]) * inv_l,
+                           __uint_as_float(ov[8 * e + 5]) * inv_l, __uint_as_float(ov[8 * e + 6]) * inv_l,
+                           __uint_as_float(ov[8 * e + 7]) * inv_l);
           }
         }
         if (write) p.casc_lse[ps] = m_used + __log2f(l);
@@ -799,6 +803,14 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (!EXTEND) {
+    // the prefix partials of this CTA are written (the barrier orders every warp's stores before this
+    // thread's fence): the decode combine merges a request's partials once every CTA has counted itself
+    if (threadIdx.x == 0) {
+      __threadfence();
+      atomicAdd(p.done_counter, 1);
+    }
+  }
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

@@ -42,7 +42,7 @@ constexpr int kMaxStages = 8;
 constexpr int kItemRing = 16;      // published items; the leader runs at most nstage + 1 items ahead
 constexpr int kProducers = 4;      // warps issuing the bulk copies of a slab (TMA issue rate grows with them)
 constexpr int kRowsPerProducer = 2 * kSlab / kProducers;  // K rows then V rows of a slab, split evenly
-constexpr int kHdrBytes = 512;     // full/empty barriers, item ring, abort flag, item barriers
+constexpr int kHdrBytes = 640;     // full/empty barriers, item ring, abort flag, item / done / free barriers
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kPlanThreads = 1024;  // one CTA plans the call
 constexpr int kRemBuckets = 64;     // size classes of the requests' last (short) items
@@ -79,9 +79,12 @@ __device__ __forceinline__ void decode_item(const DecodeParams& p, int32_t idx, 
 // -- with one cp.async.bulk each into a ring stage.  The first producer also claims the items and
 // publishes them through a shared ring (with one mbarrier per entry) as soon as it claims them, a
 // few slabs ahead, so every producer looks one slab ahead across items for its slot ids.  Consumer
-// warp w owns kv head hg * hpc + w of every item.
+// warp w owns kv head hg * hpc + w of every item.  Warp hpc+4 signals finished partials: once every
+// consumer warp is done with an item whose request goes through the combine, it makes the partials
+// visible device-wide (a gpu-scope fence) and adds one to the request's count, so the combine can merge
+// the request as soon as its count is complete -- the fence stays off the consumer warps' path.
 template <int D>
-__global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers + 1), 1) decode_kernel(const DecodeParams p) {
   constexpr int KT = D / 16;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -94,20 +97,28 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
   volatile int32_t* s_items = reinterpret_cast<volatile int32_t*>(smem + 128);
   volatile int32_t* s_abort = reinterpret_cast<volatile int32_t*>(smem + 192);
   const uint32_t item0 = sbase + 256;  // kItemRing mbarriers: entry published
+  const uint32_t done0 = sbase + 384;  // kItemRing mbarriers: every consumer warp is done with the entry
+  const uint32_t free0 = sbase + 512;  // kItemRing mbarriers: the signal warp has read the entry (slot free)
   const uint32_t stage0 = sbase + kHdrBytes;
   const int RS = p.row_stride;
-  // Let the combine launch.  Without groups the producers and consumers wait for the plan kernel before
-  // the first claim.  With groups the plan kernel made its writes visible before it let this kernel
-  // launch, and it completes only after the prefix pass: this kernel reads nothing the pass writes, so
-  // it does not wait here (it runs beside the pass).  It waits before leaving, so that its completion
-  // implies the plan's and the prefix pass's (the combine reads both passes' partials).
+  // Without groups the plan kernel is the call's first kernel: wait for it (its plan, the reset counters and
+  // a fused store) before anything else.  With groups the plan kernel made its writes visible before it let
+  // this kernel launch, and it completes only after the prefix pass: this kernel reads nothing the pass
+  // writes, so it does not wait here (it runs beside the pass).  It waits before leaving, so that its
+  // completion implies the plan's and the prefix pass's.  Then the combine may launch: the plan it reads is
+  // visible, and it waits per request for the partials it merges.
+  if (p.key_start == nullptr) griddep_wait();
   griddep_launch();
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s) {
       mbar_init(full0 + 8 * s, kProducers);
       mbar_init(empty0 + 8 * s, nc);
     }
-    for (int s = 0; s < kItemRing; ++s) mbar_init(item0 + 8 * s, 1);
+    for (int s = 0; s < kItemRing; ++s) {
+      mbar_init(item0 + 8 * s, 1);
+      mbar_init(done0 + 8 * s, nc);
+      mbar_init(free0 + 8 * s, 1);
+    }
     *s_abort = 0;
     fence_mbar_init();
   }
@@ -130,11 +141,14 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
       idx = __shfl_sync(0xffffffffu, idx, 0);
       return idx < n_claims ? idx : -1;
     };
-    auto publish = [&](int32_t n, int32_t idx) {
+    // entry n reuses the ring slot of entry n - kItemRing: the signal warp, the last reader, must have read it
+    auto publish = [&](int32_t n, int32_t idx) -> bool {
+      if (n >= kItemRing && !mbar_wait(free0 + 8 * (n % kItemRing), ((n / kItemRing) - 1) & 1)) return false;
       if (lane == 0) {
         s_items[n % kItemRing] = idx;
         mbar_arrive(item0 + 8 * (n % kItemRing));
       }
+      return true;
     };
     // 1: item n in `it`; 0: end of work; -1: a bounded wait ran out
     auto next_item = [&](int32_t n, Item& it) -> int {
@@ -151,22 +165,23 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
       key = key < nk ? key : nk - 1;
       return __ldg(p.table + static_cast<int64_t>(it.row) * p.table_stride + it.k0 + key);
     };
-    // without groups the plan (and the reset work counter) is visible once the plan kernel completes;
-    // with groups it was made visible before this kernel launched
-    if (p.key_start == nullptr) griddep_wait();
     n_claims = p.plan[0] * p.n_hgroups;
-    if (leader) publish(0, claim());
+    bool ok = true;
+    if (leader) ok = __all_sync(0xffffffffu, publish(0, claim()));
     int32_t n = 0, c = 0, s = 0;
     Item it;
-    int r = next_item(0, it);
-    bool ok = r >= 0;
+    int r = ok ? next_item(0, it) : -1;
+    ok = r >= 0;
     int32_t slot = r > 0 ? load_slot(it, 0) : 0;
     while (ok && r > 0) {
       const int32_t n_slabs = (it.k1 - it.k0 + kSlab - 1) / kSlab;
       // the leader claims the next item when this one has ns slabs left to issue: the claim overlaps
       // them, and items stay unclaimed for CTAs that start late (behind a cascade prefix pass that
       // holds their SMs) instead of queueing behind this one
-      if (leader && s == (n_slabs > ns ? n_slabs - ns : 0)) publish(n + 1, claim());
+      if (leader && s == (n_slabs > ns ? n_slabs - ns : 0) && !__all_sync(0xffffffffu, publish(n + 1, claim()))) {
+        ok = false;
+        break;
+      }
       // one slab ahead: the next (item, slab) and its slot id
       Item it2 = it;
       int32_t s2 = s + 1, n2 = n;
@@ -219,13 +234,40 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
     griddep_wait();
     return;
   }
-  if (warp >= nc + kProducers) {
+  if (warp == nc + kProducers) {
+    // ================================================================ signaller
+    for (int32_t n = 0;; ++n) {
+      const int e = n % kItemRing;
+      if (!mbar_wait(done0 + 8 * e, (n / kItemRing) & 1)) {
+        if (lane == 0) {
+          *s_abort = 1;
+          flag_error(p.err, RA_DEVERR_TIMEOUT);
+        }
+        break;
+      }
+      const int32_t idx = s_items[e];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(free0 + 8 * e);
+      if (idx < 0) break;
+      if (lane == 0) {
+        Item it;
+        decode_item(p, idx, it);
+        if (!(it.n_splits == 1 && it.start == 0)) {  // partials, merged by the combine
+          __threadfence();  // the consumers' partials (ordered before this by the done barrier) first
+          atomicAdd(p.req_done + it.b, 1);
+        }
+      }
+      __syncwarp();
+    }
+    griddep_wait();
+    return;
+  }
+  if (warp > nc + kProducers) {
     griddep_wait();
     return;
   }
 
   // ================================================================ consumers
-  if (p.key_start == nullptr) griddep_wait();  // the plan the items are decoded from is visible
   const int g = lane >> 2;  // q head within the GQA group (MMA N index)
   const int tq = lane & 3;
   const uint32_t a_off = (lane & 15) * RS + (lane >> 4) * 16 + warp * D * 2;
@@ -238,6 +280,8 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
     const int32_t idx = s_items[n % kItemRing];
     if (idx < 0) {
       clean = true;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(done0 + 8 * (n % kItemRing));  // the signal warp reads the end marker
       break;
     }
     Item it;
@@ -359,6 +403,9 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
         if (h1) p.part_lse[ps1] = m1 + __log2f(l1);
       }
     }
+    // this warp's part of the entry is written (__syncwarp orders the lanes' stores before lane 0's release)
+    __syncwarp();
+    if (lane == 0) mbar_arrive(done0 + 8 * (n % kItemRing));
   }
   if (!clean && lane == 0) {
     // a bounded wait ran out: stop the producer as well
@@ -370,18 +417,21 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers), 1) decode
 
 // Merge the partials of every request that has more than one (its private splits' and the shared-prefix
 // pass's): o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M).  One warp per (request, q head), each lane
-// owning D/32 dims.  The merge is latency-bound, so a warp keeps its loads in flight together: the
-// log-sum-exps of 32 partials (one per lane) and the first kRows private partial rows are issued at once
-// (private partials are always written), the weights follow from warp shuffles, and the other rows come
-// kRows at a time, prefix rows only where a group wrote them (a finite log-sum-exp; most of the prefix
-// slots of a request are empty).  Partials are taken private first, then prefix, in chunks of 32 folded
-// with a running maximum.
+// owning D/32 dims.  The kernel launches while the decode kernel still runs (every decode CTA has started)
+// and a warp waits only for its own request: until the request's count of (item, head group) partials is
+// complete (the decode kernel's signal warp adds to it) and, when the request has prefix partials, until
+// every CTA of the prefix pass is done.  Requests whose last items finish early are merged while the rest
+// of the decode kernel runs.  Partials are read through L2 (they were written by other SMs during this
+// call).  The merge is latency-bound, so a warp keeps its loads in flight together: the log-sum-exps of 32
+// partials (one per lane) and the first kRows private partial rows are issued at once (private partials
+// are always written), the weights follow from warp shuffles, and the other rows come kRows at a time,
+// prefix rows only where a group wrote them (a finite log-sum-exp; most of the prefix slots of a request
+// are empty).  Partials are taken private first, then prefix, in chunks of 32 folded with a running
+// maximum.
 template <int D>
-__global__ void __launch_bounds__(32 * kCombineWarps) decode_combine_kernel(const DecodeParams p) {
+__device__ __forceinline__ void merge_request_head(const DecodeParams& p) {
   constexpr int V = D / 32;
   constexpr int kRows = 8;
-  griddep_wait();  // the decode kernel (and, through it, the prefix pass) has completed
-  griddep_launch();
   const int warp_global = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (warp_global >= p.batch * p.hq) return;
@@ -389,29 +439,42 @@ __global__ void __launch_bounds__(32 * kCombineWarps) decode_combine_kernel(cons
   // the request's description, loaded together (one round trip)
   int32_t L = __ldg(p.seq_lens + b);
   const int32_t row = __ldg(p.rpi + b);
-  int32_t start = p.key_start ? __ldg(p.key_start + b) : 0;
-  const int32_t i0 = p.req_item0[b];  // the request's private items are i0 .. i0 + n_splits - 1
-  const int32_t n_splits = p.req_item0[b + 1] - i0;
+  int32_t start = p.key_start ? __ldcg(p.key_start + b) : 0;
+  const int32_t i0 = __ldcg(p.req_item0 + b);  // the request's private items are i0 .. i0 + n_splits - 1
+  const int32_t n_splits = __ldcg(p.req_item0 + b + 1) - i0;
   if (row < 0 || row >= p.table_rows || L < 1) return;
   if (L > p.max_seq_len) L = p.max_seq_len;
   start = start < 0 ? 0 : (start > L ? L : start);
   // prefix partials: every slot of every level; those no group wrote hold -inf (weight 0, skipped)
   const int32_t n_pre = start > 0 ? p.casc_slots : 0;
   if (n_splits == 1 && n_pre == 0) return;  // written directly by the decode kernel
+  // wait for this request's partials
+  const int32_t expect = n_splits * p.n_hgroups;
+  bool ready = true;
+  if (lane == 0) {
+    if (expect > 0) ready = wait_count(p.req_done + b, expect);
+    if (ready && n_pre > 0) ready = wait_count(p.prefix_done, p.prefix_ctas);
+    if (!ready) flag_error(p.err, RA_DEVERR_TIMEOUT);
+  }
+  if (!__shfl_sync(0xffffffffu, ready, 0)) return;
+  if (expect > 0) (void)ld_acquire_gpu(p.req_done + b);  // each lane's own acquire
+  if (n_pre > 0) (void)ld_acquire_gpu(p.prefix_done);
   const int32_t n = n_splits + n_pre;
   const int64_t bh = warp_global;
   const int64_t h = bh - static_cast<int64_t>(b) * p.hq;
+  const int64_t slot_stride = static_cast<int64_t>(p.batch) * p.hq;  // prefix partials: [slot][request][q head]
   auto lse_of = [&](int s) {
-    return s < n_splits ? p.part_lse[(i0 + s) * p.hq + h] : p.casc_lse[bh * p.casc_slots + (s - n_splits)];
+    return s < n_splits ? __ldcg(p.part_lse + (i0 + s) * p.hq + h)
+                        : __ldcg(p.casc_lse + (s - n_splits) * slot_stride + bh);
   };
   auto load_row = [&](int s, float (&x)[V]) {
     const float* src = (s < n_splits ? p.part_o + ((i0 + s) * p.hq + h) * D
-                                     : p.casc_o + (bh * p.casc_slots + (s - n_splits)) * D) + lane * V;
+                                     : p.casc_o + ((s - n_splits) * slot_stride + bh) * D) + lane * V;
     if constexpr (V == 4) {
-      const float4 t = *reinterpret_cast<const float4*>(src);
+      const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
       x[0] = t.x, x[1] = t.y, x[2] = t.z, x[3] = t.w;
     } else {
-      const float2 t = *reinterpret_cast<const float2*>(src);
+      const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
       x[0] = t.x, x[1] = t.y;
     }
   };
@@ -463,6 +526,15 @@ __global__ void __launch_bounds__(32 * kCombineWarps) decode_combine_kernel(cons
   for (int v = 0; v < V; v += 2)
     *reinterpret_cast<__nv_bfloat162*>(p.o + bh * D + lane * V + v) =
         __floats2bfloat162_rn(acc[v] * inv, acc[v + 1] * inv);
+}
+
+template <int D>
+__global__ void __launch_bounds__(32 * kCombineWarps) decode_combine_kernel(const DecodeParams p) {
+  griddep_launch();
+  merge_request_head<D>(p);
+  // every CTA waits before it leaves, so that this grid's completion implies the decode kernel's (and,
+  // through it, the plan kernel's and the prefix pass's): the next kernel on the stream may rely on it
+  griddep_wait();
 }
 
 // Block-wide exclusive scan of (a, b) pairs over kPlanThreads threads; totals returned in ta, tb.
@@ -599,6 +671,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
     const int32_t len = len_of(b, false);
     const int32_t c = (len + chunk - 1) / chunk, f = len / chunk, rem = len % chunk;
     p.req_item0[b] = cnt;
+    p.req_done[b] = 0;
     for (int32_t s = 0; s < c; ++s) p.item_req[cnt + s] = b;
     for (int32_t s = 0; s < f; ++s) p.order[full + s] = cnt + s;
     if (rem > 0) p.order[atomicAdd(&s_hist[static_cast<int64_t>(chunk - rem) * kRemBuckets / chunk], 1)] = cnt + f;
@@ -622,42 +695,39 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
   }
 }
 
-// Zero the workspace's integer block (work counters, key starts) at the head of a call with cascade
-// groups; with a fused store, CTAs 1.. scatter the step's new rows.
-__global__ void zero_ints_kernel(const DecodeParams p, int32_t* x, int32_t n) {
+// First kernel of a call with cascade groups.  CTA 0 clears the workspace's leading integer block (key
+// starts, the work counters, the prefix pass's completion count), then sets key_start[b] to the largest range
+// end of b's groups (0 for requests in no group); CTAs 1 .. lse_ctas set every prefix-partial log-sum-exp to
+// -inf (slots no group writes stay so); the CTAs after them run the fused store.
+__global__ void cascade_setup_kernel(const DecodeParams p, int32_t* ints, int32_t n_zero, const int32_t* group_indptr,
+                                     const int32_t* group_reqs, const int32_t* group_prefix_len, int32_t num_groups,
+                                     int64_t n_lse, int32_t lse_ctas) {
   griddep_wait();  // earlier kernels on the stream may still use the workspace and the pool
   griddep_launch();
   if (blockIdx.x == 0) {
-    for (int32_t i = threadIdx.x; i < n; i += blockDim.x) x[i] = 0;
+    for (int32_t i = threadIdx.x; i < n_zero; i += blockDim.x) ints[i] = 0;
+    __syncthreads();
+    const int32_t total = __ldg(group_indptr + num_groups);
+    for (int32_t m = threadIdx.x; m < total; m += blockDim.x) {
+      int32_t lo = 0, hi = num_groups;  // group g with indptr[g] <= m < indptr[g+1]
+      while (hi - lo > 1) {
+        const int32_t mid = (lo + hi) >> 1;
+        if (__ldg(group_indptr + mid) <= m) lo = mid; else hi = mid;
+      }
+      const int32_t b = __ldg(group_reqs + m);
+      if (b < 0 || b >= p.batch) {
+        flag_error(p.err, RA_DEVERR_TABLE);
+        continue;
+      }
+      atomicMax(ints + b, __ldg(group_prefix_len + lo));
+    }
+  } else if (static_cast<int32_t>(blockIdx.x) <= lse_ctas) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x - 1) * blockDim.x + threadIdx.x; i < n_lse;
+         i += static_cast<int64_t>(lse_ctas) * blockDim.x)
+      p.casc_lse[i] = -INFINITY;
   } else {
-    scatter_new_rows(p, static_cast<int64_t>(blockIdx.x - 1) * blockDim.x + threadIdx.x,
-                     static_cast<int64_t>(gridDim.x - 1) * blockDim.x);
-  }
-}
-
-// key_start[b] = the largest range end of b's cascade groups (0 for requests in no group, set by the
-// memset); every prefix-partial slot's log-sum-exp starts at -inf (slots no group writes stay so).
-__global__ void cascade_key_start_kernel(int32_t* key_start, int32_t batch, const int32_t* group_indptr,
-                                         const int32_t* group_reqs, const int32_t* group_prefix_len,
-                                         int32_t num_groups, float* casc_lse, int64_t n_lse, uint32_t* err) {
-  griddep_wait();
-  griddep_launch();
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n_lse;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    casc_lse[i] = -INFINITY;
-  const int32_t total = __ldg(group_indptr + num_groups);
-  for (int32_t m = blockIdx.x * blockDim.x + threadIdx.x; m < total; m += gridDim.x * blockDim.x) {
-    int32_t lo = 0, hi = num_groups;  // group g with indptr[g] <= m < indptr[g+1]
-    while (hi - lo > 1) {
-      const int32_t mid = (lo + hi) >> 1;
-      if (__ldg(group_indptr + mid) <= m) lo = mid; else hi = mid;
-    }
-    const int32_t b = __ldg(group_reqs + m);
-    if (b < 0 || b >= batch) {
-      flag_error(err, RA_DEVERR_TABLE);
-      continue;
-    }
-    atomicMax(key_start + b, __ldg(group_prefix_len + lo));
+    const int64_t cta = blockIdx.x - 1 - lse_ctas;
+    scatter_new_rows(p, cta * blockDim.x + threadIdx.x, static_cast<int64_t>(gridDim.x - 1 - lse_ctas) * blockDim.x);
   }
 }
 
@@ -673,7 +743,7 @@ ra_status launch_decode(const DecodeParams& p, int grid, int smem, cudaStream_t 
     if (e != cudaSuccess) return fail(RA_ERR_CUDA, "cudaFuncSetAttribute(decode): %s", cudaGetErrorString(e));
     configured[dev.device] = kSmemLimit;
   }
-  if (ra_status st = launch_pdl("decode_kernel", kern, dim3(grid), dim3(32 * (p.hpc + kProducers)), smem, stream, p))
+  if (ra_status st = launch_pdl("decode_kernel", kern, dim3(grid), dim3(32 * (p.hpc + kProducers + 1)), smem, stream, p))
     return st;
   const int nwarps = p.batch * p.hq;
   return launch_pdl("decode_combine_kernel", decode_combine_kernel<D>, dim3((nwarps + kCombineWarps - 1) / kCombineWarps),
@@ -707,10 +777,12 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
     const int64_t base = static_cast<int64_t>(num_groups) * num_kv_heads * mtiles;
     const int64_t tiles = (max_group_prefix_len + 127) / 128;
     // CTAs per wave: GB300's 152 SMs in the share the shared prefix takes of the longest context (the
-    // host-side bounds), at least two thirds of them; the rest run the private decode beside the pass.
-    // Measured: a forked batch (8192 shared + <= 257 private keys) 64 -> 58 us with all SMs for the
-    // pass, while the 8B-shape batch (1024 shared of <= 4096) loses 10% unless a third is left to its
-    // private keys.  Computed from the call's bounds, not the device: the workspace size (sized on the
+    // host-side bounds), at least two thirds of them; the pass's grid is capped at the wave, and the rest
+    // run the private decode beside the pass.  Measured: a forked batch (8192 shared + <= 257 private
+    // keys) 64 -> 58 us with all SMs for the pass, while the 8B-shape batch (1024 shared of <= 4096) loses
+    // 10% unless a third is left to its private keys; the multi-turn mix (prefixes up to 13.7K of 32K)
+    // takes 223 us with the grid capped at 104 CTAs, 230 us with all 152, 225-244 us with a wave of
+    // 88 / 76 / 64.  Computed from the call's bounds, not the device: the workspace size (sized on the
     // host, possibly with no device current) must not depend on which device runs the call.
     const int64_t share = 152 * static_cast<int64_t>(max_group_prefix_len) / (max_seq_len > 0 ? max_seq_len : 1);
     const int64_t sms = share < 104 ? 104 : (share > 152 ? 152 : share);
@@ -726,6 +798,7 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
     }
     if (best_tiles > tiles) best_tiles = tiles;
     pl.cchunk = static_cast<int32_t>(best_tiles * 128);
+    pl.prefix_wave = static_cast<int32_t>(sms);
     pl.max_csplits = static_cast<int32_t>((max_group_prefix_len + pl.cchunk - 1) / pl.cchunk);
   }
   return pl;
@@ -751,9 +824,9 @@ DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int3
   }
   w.ints = off;
   (void)num_kv_heads;
-  w.zero_bytes = (static_cast<size_t>(batch) + 2) * sizeof(int32_t);
-  w.ints_bytes = w.zero_bytes + (2 + static_cast<size_t>(batch) + 1 + 2 * static_cast<size_t>(pl.max_items)) *
-                                    sizeof(int32_t);
+  w.zero_bytes = (static_cast<size_t>(batch) + 3) * sizeof(int32_t);
+  w.ints_bytes = w.zero_bytes + (2 + static_cast<size_t>(batch) + 1 + 2 * static_cast<size_t>(pl.max_items) +
+                                 static_cast<size_t>(batch)) * sizeof(int32_t);
   off += up(w.ints_bytes);
   w.total = off;
   return w;
@@ -877,34 +950,35 @@ static ra_status decode_call(const void* k_pool, const void* v_pool, int64_t num
   int32_t* ints = reinterpret_cast<int32_t*>(ws + wl.ints);
   p.counter = ints + batch;
   p.prefix_counter = ints + batch + 1;
-  p.plan = ints + batch + 2;
+  p.prefix_done = ints + batch + 2;
+  p.plan = ints + batch + 3;
   p.req_item0 = p.plan + 2;
   p.item_req = p.req_item0 + batch + 1;
   p.order = p.item_req + pl.max_items;
+  p.req_done = p.order + pl.max_items;
   // Kernels rather than memsets, so that the launches of the call stay chained programmatically:
-  // with groups, [zero key starts and counters] -> [key-start scatter] -> [prefix pass] -> [plan] ->
+  // with groups, [set-up: counters, key starts, empty prefix partials] -> [prefix pass] -> [plan] ->
   // [decode] -> [combine]; without, [plan] -> [decode] -> [combine].
   if (num_groups > 0) {
     p.cchunk = pl.cchunk;
     p.max_csplits = pl.max_csplits;
+    p.prefix_wave = pl.prefix_wave;
     p.casc_slots = levels * pl.max_csplits;
     p.casc_o = reinterpret_cast<float*>(ws + wl.casc_o);
     p.casc_lse = reinterpret_cast<float*>(ws + wl.casc_lse);
     p.key_start = ints;
-    if (ra_status st = launch_pdl("zero_ints_kernel", zero_ints_kernel, dim3(1 + store_ctas), dim3(256), 0, s, p,
-                                  ints, static_cast<int32_t>(wl.zero_bytes / sizeof(int32_t))))
+    const int64_t n_lse = static_cast<int64_t>(batch) * num_q_heads * p.casc_slots;
+    const int64_t lse_want = (n_lse + 256 * 8 - 1) / (256 * 8);  // ~8 values per thread
+    const int32_t lse_ctas = static_cast<int32_t>(lse_want < 128 ? (lse_want > 0 ? lse_want : 1) : 128);
+    if (ra_status st = launch_pdl("cascade_setup_kernel", cascade_setup_kernel, dim3(1 + lse_ctas + store_ctas),
+                                  dim3(256), 0, s, p, ints, static_cast<int32_t>(wl.zero_bytes / sizeof(int32_t)),
+                                  group_indptr, group_reqs, group_prefix_len, num_groups, n_lse, lse_ctas))
       return st;
-    if (ra_status st = launch_pdl("cascade_key_start_kernel", cascade_key_start_kernel, dim3((batch + 127) / 128),
-                                  dim3(128), 0, s, ints, batch, group_indptr, group_reqs, group_prefix_len, num_groups,
-                                  p.casc_lse, static_cast<int64_t>(batch) * num_q_heads * p.casc_slots, device_error))
-      return st;
-  }
-  if (num_groups > 0) {
     CascadeArgs ca{group_indptr,         group_reqs,           group_prefix_start, group_prefix_len, group_level,
                    num_groups,           max_group_prefix_len, max_group_size,     max_group_levels};
-    if (ra_status st = launch_cascade_prefix(p, ca, head_dim, s)) return st;
+    if (ra_status st = launch_cascade_prefix(p, ca, head_dim, s, &p.prefix_ctas)) return st;
   }
-  // (with groups the zeroing kernel did the fused store: the plan kernel runs behind the prefix pass)
+  // (with groups the set-up kernel did the fused store: the plan kernel runs behind the prefix pass)
   if (ra_status st = launch_pdl("decode_plan_kernel", decode_plan_kernel, dim3(1 + (num_groups > 0 ? 0 : store_ctas)),
                                 dim3(kPlanThreads), 0, s, p))
     return st;

@@ -39,6 +39,10 @@ struct DecodeParams {
   int32_t max_items;         // kDecodePlanItems + batch: bound of the plan's items
   int32_t* counter;          // work-item counter (reset by the plan kernel)
   int32_t* prefix_counter;   // cascade prefix pass's work-item counter (zeroed with the key starts)
+  int32_t* prefix_done;      // cascade prefix pass: CTAs that have written all their partials (zeroed likewise)
+  int32_t prefix_ctas;       // cascade prefix pass: CTAs launched
+  int32_t prefix_wave;       // cascade prefix pass: the wave size its splits were planned for
+  int32_t* req_done;         // [batch]: (item, head group) partials written per request (reset by the plan kernel)
   int32_t* plan;             // [2]: items, keys per item (chunk), written by the plan kernel
   int32_t* req_item0;        // [batch + 1]: request b's items are req_item0[b] .. req_item0[b+1]-1
   int32_t* item_req;         // [max_items]: request of each item
@@ -48,8 +52,8 @@ struct DecodeParams {
   int32_t cchunk;      // shared-prefix keys per prefix-pass split (cascade)
   int32_t max_csplits;  // prefix-pass splits per group range
   int32_t casc_slots;   // prefix partials per (request, q head): levels x max_csplits
-  float* casc_o;        // [batch, hq, casc_slots, D] shared-prefix partials (cascade)
-  float* casc_lse;      // [batch, hq, casc_slots]; -inf marks a slot no group wrote
+  float* casc_o;        // [casc_slots, batch, hq, D] shared-prefix partials (cascade)
+  float* casc_lse;      // [casc_slots, batch, hq]; -inf marks a slot no group wrote
   uint32_t* err;
   // fused store (ra_decode_attention_store): the step's new rows, scattered by the call's first kernel
   const uint4* st_k;       // [batch, hkv, D] bf16 as 16-byte vectors, or nullptr (no store)
@@ -71,12 +75,14 @@ struct DecodePlan {
   int32_t max_items = 0;    // kDecodePlanItems + batch
   int32_t cchunk = 0;       // shared-prefix keys per prefix-pass split (cascade)
   int32_t max_csplits = 0;
+  int32_t prefix_wave = 0;  // prefix-pass CTAs (of GB300's 152 SMs) the cost model planned the splits for
 };
 
 struct DecodeWorkspace {
   size_t part_o = 0, part_lse = 0, casc_o = 0, casc_lse = 0;
-  size_t ints = 0, ints_bytes = 0;  // key_start [batch], counter, prefix counter (zeroed with groups);
-                                    // plan [2], req_item0 [batch+1], item_req, order [max_items]
+  size_t ints = 0, ints_bytes = 0;  // key_start [batch], counter, prefix counter, prefix done (zeroed with
+                                    // groups); plan [2], req_item0 [batch+1], item_req, order [max_items],
+                                    // req_done [batch]
   size_t zero_bytes = 0;            // leading part of the block cleared before the key-start scatter
   size_t total = 0;
 };
@@ -102,7 +108,8 @@ DecodeWorkspace layout_decode_workspace(int32_t batch, int32_t num_q_heads, int3
 
 // Tensor-core pass over each group's shared prefix: writes p.casc_o / p.casc_lse
 // for every member (defined with the tcgen05 attention kernel).
+// Returns the pass's grid size in *ctas (each of its CTAs adds one to p.prefix_done when it is done).
 ra_status launch_cascade_prefix(const DecodeParams& p, const CascadeArgs& ca, int32_t head_dim,
-                                cudaStream_t stream);
+                                cudaStream_t stream, int32_t* ctas);
 
 }  // namespace ra

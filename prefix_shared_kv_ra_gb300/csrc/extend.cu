@@ -221,7 +221,7 @@ ra_status launch_extend(const TcParams& p, const CUtensorMap& qmap, int64_t entr
 }
 
 template <int D>
-ra_status launch_prefix(const TcParams& p, int grid_x, int num_groups, cudaStream_t s) {
+ra_status launch_prefix(const TcParams& p, int grid_x, int num_groups, int32_t wave, cudaStream_t s, int32_t* ctas) {
   using L = tc::Layout<D, k_stages<D>(), v_stages<D>()>;
   auto kern = attn_tc_kernel<D, k_stages<D>(), v_stages<D>(), false>;
   static bool configured[64] = {};
@@ -236,7 +236,12 @@ ra_status launch_prefix(const TcParams& p, int grid_x, int num_groups, cudaStrea
   if (ra_status st = row_gather_map(&vmap, p.v_pool, p.num_slots * p.hkv, D)) return st;
   // persistent: one CTA per SM (at most one per item)
   const int64_t items = static_cast<int64_t>(grid_x) * p.hkv * num_groups;
-  dim3 grid(static_cast<unsigned>(items < dev.num_sms ? items : dev.num_sms));
+  // at most the wave the splits were planned for: the SMs beyond it run the private decode beside the pass
+  // (multi-turn mix: 230 -> 223 us for the decode call, the other workloads unchanged)
+  int64_t cap = dev.num_sms;
+  if (wave > 0 && wave < cap) cap = wave;
+  dim3 grid(static_cast<unsigned>(items < cap ? items : cap));
+  *ctas = static_cast<int32_t>(grid.x);
   return launch_pdl("attn_tc_kernel<cascade prefix>", kern, grid, dim3(tc::kThreads), L::kDynSmem, s, p, qmap, kmap,
                     vmap);
 }
@@ -244,7 +249,7 @@ ra_status launch_prefix(const TcParams& p, int grid_x, int num_groups, cudaStrea
 }  // namespace
 
 ra_status launch_cascade_prefix(const DecodeParams& d, const CascadeArgs& ca, int32_t head_dim,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, int32_t* ctas) {
   if (128 % d.group != 0)
     return fail(RA_ERR_UNSUPPORTED, "GQA group %d does not divide the 128-row tile", d.group);
   TcParams p{};
@@ -275,13 +280,14 @@ ra_status launch_cascade_prefix(const DecodeParams& d, const CascadeArgs& ca, in
   p.casc_o = d.casc_o;
   p.casc_lse = d.casc_lse;
   p.work_counter = d.prefix_counter;
+  p.done_counter = d.prefix_done;
   p.num_groups = ca.num_groups;
   const int members_per_cta = tc::kTiles * (128 / d.group);
   const int mtiles = (ca.max_group_size + members_per_cta - 1) / members_per_cta;
   const int grid_x = mtiles * d.max_csplits;
   p.grid_x = grid_x;
-  return head_dim == 128 ? launch_prefix<128>(p, grid_x, ca.num_groups, stream)
-                         : launch_prefix<64>(p, grid_x, ca.num_groups, stream);
+  return head_dim == 128 ? launch_prefix<128>(p, grid_x, ca.num_groups, d.prefix_wave, stream, ctas)
+                         : launch_prefix<64>(p, grid_x, ca.num_groups, d.prefix_wave, stream, ctas);
 }
 
 }  // namespace ra
