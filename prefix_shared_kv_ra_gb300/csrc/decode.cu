@@ -657,13 +657,17 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(const DecodeP
   }
   int32_t n_items, n_full;
   plan_scan2(cnt, full, n_items, n_full, s_wa, s_wb);
-  if (t == 0) {  // bucket starts, largest remainders first, after the full items
-    int32_t acc = n_full;
-    for (int k = 0; k < kRemBuckets; ++k) {
-      const int32_t c = s_hist[k];
-      s_hist[k] = acc;
-      acc += c;
+  if (t < 32) {  // bucket starts, largest remainders first, after the full items: a warp scan, 2 buckets a lane
+    const int32_t c0 = s_hist[2 * t], c1 = s_hist[2 * t + 1];
+    int32_t incl = c0 + c1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (t >= off) incl += y;
     }
+    const int32_t excl = n_full + incl - (c0 + c1);
+    s_hist[2 * t] = excl;
+    s_hist[2 * t + 1] = excl + c0;
   }
   __syncthreads();
   if (!behind_pass) griddep_wait();  // the workspace is free
