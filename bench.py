@@ -36,7 +36,8 @@ METRIC = "attn tokens/s; decode KV GB/s and extend TFLOP/s as % of GB300 rooflin
 UNIT = "tokens/s"
 WORKLOAD = ("multi-turn chat mix, 70B heads (64 q / 8 kv, head_dim 128, bf16): 256 requests, lognormal "
             "contexts (median 2048, clipped 16..32768), radix-tree prefix sharing at 70% token hit ratio; "
-            "32 extend (suffix 64..512) + 224 decode (cascade groups from the radix tree); pool 2M slots")
+            "32 extend (suffix 64..512) + 224 decode in the tree's depth-first order (cascade groups from the radix "
+            "tree); pool 2M slots")
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -189,6 +190,33 @@ class ClockSampler:
         reasons = sorted({n for _, _, flags in rows for n, v in zip(names, flags) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
                 "reasons": reasons, "samples": len(rows)}
+
+
+def schedule_decode_dfs(b):
+    """The batch with its decode requests in the radix tree's depth-first order (radix.dfs_order), as a
+    cache-aware scheduler runs it: requests that share slots beyond their group's prefix are adjacent, so
+    the decode kernel's items read those slots close together in time.  Queries, lengths, table rows and
+    the requests' new-token rows (store inputs) are permuted together; the extend part is unchanged."""
+    import copy
+    from prefix_shared_kv_ra_gb300.radix import dfs_order
+    rows = [b.req_to_token[r, :L] for r, L in zip(b.dec_rpi, b.dec_seq_lens)]
+    order = dfs_order(rows)
+    c = copy.copy(b)
+    c.dec_rpi, c.dec_seq_lens, c.dec_q = b.dec_rpi[order], b.dec_seq_lens[order], b.dec_q[order]
+    n0 = b.total_q_extend  # new tokens: the extend suffixes, then one per decode request
+    perm = np.concatenate([np.arange(n0), n0 + order])
+    c.out_cache_loc, c.k_new, c.v_new = b.out_cache_loc[perm], b.k_new[perm], b.v_new[perm]
+    c.casc_group_indptr = c.casc_group_reqs = c.casc_group_prefix_len = None
+    c.casc_group_start = c.casc_group_level = None
+    c.casc_levels = 1
+    return c
+
+
+def mix_step_batch(seed: int = 5):
+    """The benchmark's batch: the multi-turn mix with its decode requests in the tree's depth-first order
+    and the one-level cascade groups the tree derives from them."""
+    import workloads as W
+    return with_tree_groups(schedule_decode_dfs(W.multiturn_mix_70b(seed=seed)))
 
 
 def with_tree_groups(b, min_prefix: int = 256, multilevel: bool = False):
@@ -520,7 +548,7 @@ def run_reference(args):
     them) on the GPU arm's workload, one whole step per timed step on the host cores."""
     import workloads as W
     import oracle
-    b = with_tree_groups(W.multiturn_mix_70b(seed=5))
+    b = mix_step_batch(seed=5)
     pool = oracle.pool_after_store(b)
     for _ in range(args.warmup):  # the CPU has nothing to warm beyond its first pass: short warm-up steps
         oracle_step(b, pool, fraction=min(args.ref_fraction, 1.0 / 16))
@@ -559,9 +587,12 @@ def run_profile_case(name: str, steps: int):
     ra.load()
     cfg, cascade = PROFILE_CASES[name]
     dev = torch.device("cuda:0")
-    b = W.WORKLOADS[cfg]()
-    if cascade and not b.has_cascade():
-        b = with_tree_groups(b)
+    if cfg == "multiturn_mix_70b":
+        b = mix_step_batch()  # the benchmark's own batch (its groups are used only with the cascade)
+    else:
+        b = W.WORKLOADS[cfg]()
+        if cascade and not b.has_cascade():
+            b = with_tree_groups(b)
     st = Step(b, dev, cascade=cascade)
     for _ in range(steps):
         st.run()
@@ -630,7 +661,7 @@ def main():
 
     # independent replicas: each rank draws its own batch of the same workload; the decode requests are
     # grouped by the radix tree (one-level cascade groups over shared prefixes of >= 256 tokens)
-    b = with_tree_groups(W.multiturn_mix_70b(seed=5 + rank))
+    b = mix_step_batch(seed=5 + rank)
     step = Step(b, dev, cascade=True)
     flush = L2Flush(dev)
     uuid = None

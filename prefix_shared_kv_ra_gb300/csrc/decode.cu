@@ -422,12 +422,12 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers + 1), 1) de
 // complete (the decode kernel's signal warp adds to it) and, when the request has prefix partials, until
 // every CTA of the prefix pass is done.  Requests whose last items finish early are merged while the rest
 // of the decode kernel runs.  Partials are read through L2 (they were written by other SMs during this
-// call).  The merge is latency-bound, so a warp keeps its loads in flight together: the log-sum-exps of 32
-// partials (one per lane) and the first kRows private partial rows are issued at once (private partials
-// are always written), the weights follow from warp shuffles, and the other rows come kRows at a time,
-// prefix rows only where a group wrote them (a finite log-sum-exp; most of the prefix slots of a request
-// are empty).  Partials are taken private first, then prefix, in chunks of 32 folded with a running
-// maximum.
+// call).  The merge is latency-bound, so a warp keeps its loads in flight together: the request's
+// description with both counts, then the log-sum-exps of 32 partials (one per lane) with the first kRows
+// rows known to be written (private partials always are; with one-level groups so are the first
+// ceil(key_start / cchunk) prefix slots), the weights from warp shuffles, and the other rows kRows at a
+// time -- with multi-level groups, prefix rows only where a group wrote them (a finite log-sum-exp).
+// Partials are taken private first, then prefix, in chunks of 32 folded with a running maximum.
 template <int D>
 __device__ __forceinline__ void merge_request_head(const DecodeParams& p) {
   constexpr int V = D / 32;
@@ -436,30 +436,41 @@ __device__ __forceinline__ void merge_request_head(const DecodeParams& p) {
   const int lane = threadIdx.x & 31;
   if (warp_global >= p.batch * p.hq) return;
   const int b = warp_global / p.hq;
-  // the request's description, loaded together (one round trip)
+  // the request's description and, on lane 0, both counts, loaded together (one round trip)
   int32_t L = __ldg(p.seq_lens + b);
   const int32_t row = __ldg(p.rpi + b);
   int32_t start = p.key_start ? __ldcg(p.key_start + b) : 0;
   const int32_t i0 = __ldcg(p.req_item0 + b);  // the request's private items are i0 .. i0 + n_splits - 1
-  const int32_t n_splits = __ldcg(p.req_item0 + b + 1) - i0;
+  const int32_t i1 = __ldcg(p.req_item0 + b + 1);
+  int32_t done_seen = 0, pre_seen = 0;
+  if (lane == 0) {
+    done_seen = ld_relaxed_gpu(p.req_done + b);
+    if (p.key_start) pre_seen = ld_relaxed_gpu(p.prefix_done);
+  }
+  const int32_t n_splits = i1 - i0;
   if (row < 0 || row >= p.table_rows || L < 1) return;
   if (L > p.max_seq_len) L = p.max_seq_len;
   start = start < 0 ? 0 : (start > L ? L : start);
-  // prefix partials: every slot of every level; those no group wrote hold -inf (weight 0, skipped)
-  const int32_t n_pre = start > 0 ? p.casc_slots : 0;
+  // prefix partials: with one-level groups the slots the pass wrote, else every slot of every level (those
+  // no group wrote hold -inf: weight 0, skipped)
+  const int32_t n_pre = start > 0 ? (p.casc_one_level ? (start + p.cchunk - 1) / p.cchunk : p.casc_slots) : 0;
   if (n_splits == 1 && n_pre == 0) return;  // written directly by the decode kernel
-  // wait for this request's partials
+  // wait for this request's partials: lane 0 polls; then every lane reads both counts itself and fences,
+  // so that each lane's own loads of the partials follow an acquire of the counts it saw complete
   const int32_t expect = n_splits * p.n_hgroups;
   bool ready = true;
   if (lane == 0) {
-    if (expect > 0) ready = wait_count(p.req_done + b, expect);
-    if (ready && n_pre > 0) ready = wait_count(p.prefix_done, p.prefix_ctas);
+    if (expect > 0 && done_seen < expect) ready = wait_count(p.req_done + b, expect);
+    if (ready && n_pre > 0 && pre_seen < p.prefix_ctas) ready = wait_count(p.prefix_done, p.prefix_ctas);
     if (!ready) flag_error(p.err, RA_DEVERR_TIMEOUT);
   }
   if (!__shfl_sync(0xffffffffu, ready, 0)) return;
-  if (expect > 0) (void)ld_acquire_gpu(p.req_done + b);  // each lane's own acquire
-  if (n_pre > 0) (void)ld_acquire_gpu(p.prefix_done);
+  if (expect > 0) (void)ld_relaxed_gpu(p.req_done + b);
+  if (n_pre > 0) (void)ld_relaxed_gpu(p.prefix_done);
+  fence_acq_rel_gpu();
   const int32_t n = n_splits + n_pre;
+  // partials known to be written: their rows are loaded with the log-sum-exps, the others once weighed
+  const int32_t n_written = p.casc_one_level ? n : n_splits;
   const int64_t bh = warp_global;
   const int64_t h = bh - static_cast<int64_t>(b) * p.hq;
   const int64_t slot_stride = static_cast<int64_t>(p.batch) * p.hq;  // prefix partials: [slot][request][q head]
@@ -488,7 +499,7 @@ __device__ __forceinline__ void merge_request_head(const DecodeParams& p) {
     float x[kRows][V];
 #pragma unroll
     for (int k = 0; k < kRows; ++k)
-      if (k < cnt && base + k < n_splits) load_row(base + k, x[k]);  // private: written, load at once
+      if (k < cnt && base + k < n_written) load_row(base + k, x[k]);  // written: load at once
     float mc = ls;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, off));
@@ -505,7 +516,7 @@ __device__ __forceinline__ void merge_request_head(const DecodeParams& p) {
 #pragma unroll
       for (int k = 0; k < kRows; ++k) {
         const int s = base + k0 + k;
-        const bool loaded = k0 == 0 && s < n_splits;
+        const bool loaded = k0 == 0 && s < n_written;
         const float w = __shfl_sync(0xffffffffu, wl, (k0 + k) & 31);
         if (k0 + k < cnt && w > 0.f && !loaded) load_row(s, x[k]);
       }
@@ -968,6 +979,7 @@ static ra_status decode_call(const void* k_pool, const void* v_pool, int64_t num
     p.max_csplits = pl.max_csplits;
     p.prefix_wave = pl.prefix_wave;
     p.casc_slots = levels * pl.max_csplits;
+    p.casc_one_level = (max_group_levels == 1 && group_prefix_start == nullptr) ? 1 : 0;
     p.casc_o = reinterpret_cast<float*>(ws + wl.casc_o);
     p.casc_lse = reinterpret_cast<float*>(ws + wl.casc_lse);
     p.key_start = ints;

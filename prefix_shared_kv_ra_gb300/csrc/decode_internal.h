@@ -52,6 +52,8 @@ struct DecodeParams {
   int32_t cchunk;      // shared-prefix keys per prefix-pass split (cascade)
   int32_t max_csplits;  // prefix-pass splits per group range
   int32_t casc_slots;   // prefix partials per (request, q head): levels x max_csplits
+  int32_t casc_one_level;  // every group starts at position 0 at level 0: a member's written prefix partials
+                           // are exactly slots 0 .. ceil(key_start / cchunk) - 1
   float* casc_o;        // [casc_slots, batch, hq, D] shared-prefix partials (cascade)
   float* casc_lse;      // [casc_slots, batch, hq]; -inf marks a slot no group wrote
   uint32_t* err;

@@ -76,18 +76,22 @@ __device__ __forceinline__ void st_global_v8(float* dst, float a0, float a1, flo
 }
 
 // ---------------------------------------------------------------- counters shared between CTAs
-__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
+__device__ __forceinline__ int32_t ld_relaxed_gpu(const int32_t* p) {
   int32_t v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-// Wait until *ctr >= target (acquire: the writes released before the increments are visible afterwards);
-// false on deadline.  The counter is written by other CTAs of this grid or of a grid already resident.
+// After relaxed loads that observed released counts: with this fence they form an acquire, so the writes
+// released before the counts were raised are visible to this thread's later loads.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Wait until *ctr >= target, polling with relaxed loads (follow with fence_acq_rel_gpu); false on
+// deadline.  The counter is written by other CTAs of this grid or of a grid already resident.
 __device__ __forceinline__ bool wait_count(const int32_t* ctr, int32_t target) {
-  if (ld_acquire_gpu(ctr) >= target) return true;
+  if (ld_relaxed_gpu(ctr) >= target) return true;
   const long long t0 = clock64();
-  while (ld_acquire_gpu(ctr) < target) {
+  while (ld_relaxed_gpu(ctr) < target) {
     if (clock64() - t0 > kWaitDeadlineCycles) return false;
     __nanosleep(256);
   }

@@ -255,6 +255,15 @@ class RadixCache:
         return sorted(out)
 
 
+def dfs_order(paths: Sequence[Sequence[int]]) -> np.ndarray:
+    """The order in which a depth-first walk of the radix tree of these slot rows meets the requests:
+    requests sorted lexicographically by their slot rows (a node's children are visited by their first
+    slot, a request that ends at a node before the requests below it).  A scheduler that runs a batch in
+    this order keeps requests that share a node next to each other, so their shared slots are read
+    close together in time (the pages' cache-aware scheduling serves requests in this order)."""
+    return np.asarray(sorted(range(len(paths)), key=lambda b: tuple(int(x) for x in paths[b])), np.int64)
+
+
 def cascade_groups(paths: Sequence[Sequence[int]], min_prefix: int = 1,
                    min_members: int = 2) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
     """One-level cascade groups for a decode batch from its table rows.

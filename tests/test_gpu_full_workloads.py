@@ -15,7 +15,7 @@ import torch
 
 import oracle
 import workloads as W
-from helpers import DeviceBatch, assert_close, attach_tree_groups, check_store, to_f64
+from helpers import DeviceBatch, assert_close, check_store, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -69,10 +69,11 @@ def test_fewshot_extend_whole():
 
 
 def test_multiturn_mix_step_whole():
-    """The benchmark's step on its own batch: store (9.4K new tokens into a 2M-slot pool), extend of the 32
-    extend requests (all 588,480 rows), cascade decode of the 224 decode requests with the tree's groups
-    (all 14,336 rows), and the same decode without groups."""
-    b = attach_tree_groups(W.multiturn_mix_70b())
+    """The benchmark's step on its own batch (decode requests in the tree's depth-first order): store (9.4K
+    new tokens into a 2M-slot pool), extend of the 32 extend requests (all 588,480 rows), cascade decode of
+    the 224 decode requests with the tree's groups (all 14,336 rows), and the same decode without groups."""
+    import bench
+    b = bench.mix_step_batch()
     assert b.has_cascade()
     db = DeviceBatch(b)
     check_store(db)

@@ -478,3 +478,42 @@ def test_slot_pool_against_a_list_model(page):
             pool.free(held[0])                                         # the same pages again
     with pytest.raises(ValueError):
         pool.free([0])                                                 # the reserved page
+
+
+# ---------------------------------------------------------------- depth-first order of a batch
+def _trie_dfs(paths):
+    """Brute force: build a trie of the slot rows, walk it depth first (children by slot, a request that
+    ends at a node before the requests below it) and list the requests in the order met."""
+    root = {"children": {}, "ends": []}
+    for b, row in enumerate(paths):
+        node = root
+        for x in row:
+            node = node["children"].setdefault(int(x), {"children": {}, "ends": []})
+        node["ends"].append(b)
+    out = []
+
+    def walk(node):
+        out.extend(node["ends"])
+        for x in sorted(node["children"]):
+            walk(node["children"][x])
+    walk(root)
+    return out
+
+
+def test_dfs_order_matches_a_trie_walk():
+    from prefix_shared_kv_ra_gb300.radix import dfs_order
+    rng = np.random.default_rng(7)
+    for _ in range(30):
+        base = [rng.integers(0, 50, size=rng.integers(1, 12)).tolist() for _ in range(4)]
+        paths = []
+        for _ in range(int(rng.integers(1, 15))):
+            p = list(base[int(rng.integers(0, 4))])[: int(rng.integers(1, 12))]
+            p += rng.integers(0, 50, size=int(rng.integers(0, 5))).tolist()
+            paths.append(p)
+        assert dfs_order(paths).tolist() == _trie_dfs(paths)
+
+
+def test_dfs_order_puts_sharing_requests_next_to_each_other():
+    from prefix_shared_kv_ra_gb300.radix import dfs_order
+    paths = [[9, 1, 2], [5, 6], [9, 1, 3], [5, 7], [9, 4]]
+    assert dfs_order(paths).tolist() == [1, 3, 0, 2, 4]
