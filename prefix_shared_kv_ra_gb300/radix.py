@@ -260,7 +260,9 @@ def dfs_order(paths: Sequence[Sequence[int]]) -> np.ndarray:
     requests sorted lexicographically by their slot rows (a node's children are visited by their first
     slot, a request that ends at a node before the requests below it).  A scheduler that runs a batch in
     this order keeps requests that share a node next to each other, so their shared slots are read
-    close together in time (the pages' cache-aware scheduling serves requests in this order)."""
+    close together in time.  The SGLang paper summary (§3, cache-aware scheduling; A.3, proof of
+    Theorem 3.1) schedules longest shared prefix first and shows that order equivalent to a depth-first
+    walk of the radix tree."""
     return np.asarray(sorted(range(len(paths)), key=lambda b: tuple(int(x) for x in paths[b])), np.int64)
 
 
