@@ -250,6 +250,18 @@ ra_status ra_decode_attention_static(const void* k_pool, const void* v_pool, int
                                      int32_t max_group_size, int32_t max_group_levels, uint32_t* device_error,
                                      ra_stream_t stream);
 
+/*
+ * ra_selftest_bounded_wait -- check, on the current device, that a wait inside a kernel that runs out
+ * returns instead of hanging.  The pages have no counterpart: every wait in this library's kernels (on
+ * an mbarrier or on a counter another CTA raises) is bounded by a clock deadline, after which the kernel
+ * flags RA_DEVERR_TIMEOUT and leaves; this call runs one CTA that waits, with a deadline of
+ * deadline_cycles SM clock cycles (1 .. 2^32), on an mbarrier no thread arrives at and on a counter no
+ * thread raises.  Both waits run out: the kernel OR-s RA_DEVERR_TIMEOUT into *device_error (a device
+ * word, 4-byte aligned, that the caller zeroes and reads back) and returns.  Enqueues one kernel on
+ * `stream`; nothing else is touched.
+ */
+ra_status ra_selftest_bounded_wait(int64_t deadline_cycles, uint32_t* device_error, ra_stream_t stream);
+
 /* Static description of a status code. */
 const char* ra_status_string(ra_status status);
 
@@ -259,7 +271,7 @@ const char* ra_last_error_message(void);
 /* ABI revision of this header (bumped on any signature change). */
 int32_t ra_abi_version(void);
 
-#define RA_ABI_VERSION 4
+#define RA_ABI_VERSION 5
 
 #ifdef __cplusplus
 }

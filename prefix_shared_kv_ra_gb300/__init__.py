@@ -25,7 +25,7 @@ from . import _build
 __all__ = ["RAError", "ra_kv_store", "ra_extend_attention", "ra_extend_workspace_bytes", "ra_decode_attention",
            "ra_decode_workspace_bytes", "ra_decode_attention_store",
            "ra_decode_attention_static", "RA_DECODE_STATIC_SCRATCH_BYTES",
-           "ra_abi_version", "library_path", "load", "DEVERR_SLOT", "DEVERR_TABLE", "DEVERR_LENGTH",
+           "ra_abi_version", "ra_selftest_bounded_wait", "library_path", "load", "DEVERR_SLOT", "DEVERR_TABLE", "DEVERR_LENGTH",
            "DEVERR_TIMEOUT"]
 
 RA_OK = 0
@@ -68,6 +68,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     lib.ra_decode_attention_static.argtypes = [P, P, i64, i32, i32, P, P, i32, f32, P, i64, i64, P, P, i32, i32,
                                                i32, P, P, P, P, P, i32, i32, i32, P, P]
     lib.ra_decode_attention_static.restype = ctypes.c_int
+    lib.ra_selftest_bounded_wait.argtypes = [i64, P, P]
+    lib.ra_selftest_bounded_wait.restype = ctypes.c_int
     lib.ra_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32]
     lib.ra_decode_workspace_bytes.restype = sz
     for f in (lib.ra_kv_store, lib.ra_extend_attention, lib.ra_decode_attention, lib.ra_abi_version):
@@ -101,6 +103,15 @@ def _ptr(t: Optional[torch.Tensor], dtype: torch.dtype, name: str, device: torch
 def _stream(device: torch.device, stream) -> ctypes.c_void_p:
     s = stream if stream is not None else torch.cuda.current_stream(device)
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def ra_selftest_bounded_wait(deadline_cycles: int, device_error: torch.Tensor, stream=None) -> None:
+    """One kernel whose waits (an mbarrier nobody arrives at, a counter nobody raises) run out after
+    deadline_cycles SM cycles: it must flag DEVERR_TIMEOUT in device_error (int32 [1] on the GPU) and
+    return."""
+    dev = device_error.device
+    _check(load().ra_selftest_bounded_wait(int(deadline_cycles), _ptr(device_error, torch.int32, "device_error", dev),
+                                           _stream(dev, stream)))
 
 
 def ra_abi_version() -> int:

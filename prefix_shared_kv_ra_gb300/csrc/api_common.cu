@@ -2,6 +2,7 @@
 #include <mutex>
 
 #include "api_common.h"
+#include "ra_ptx.cuh"
 
 namespace ra {
 
@@ -64,3 +65,35 @@ extern "C" const char* ra_status_string(ra_status status) {
 extern "C" const char* ra_last_error_message(void) { return ra::g_last_error; }
 
 extern "C" int32_t ra_abi_version(void) { return RA_ABI_VERSION; }
+
+namespace ra {
+namespace {
+
+__device__ int32_t g_never_counted = 0;  // no thread ever writes it
+
+// One CTA: warp 0 waits on an mbarrier no thread arrives at, warp 1 on a counter no thread raises, both
+// with the caller's deadline and the same bounded-wait primitives every kernel of the library uses.
+// Both waits run out; each warp flags RA_DEVERR_TIMEOUT and the kernel returns.
+__global__ void selftest_bounded_wait_kernel(long long deadline, uint32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const bool ok = threadIdx.x < 32 ? mbar_wait(smem_u32(&bar), 0, deadline)
+                                   : wait_count(&g_never_counted, 1, deadline);
+  if (!ok && (threadIdx.x & 31) == 0) flag_error(err, RA_DEVERR_TIMEOUT);
+}
+
+}  // namespace
+}  // namespace ra
+
+extern "C" ra_status ra_selftest_bounded_wait(int64_t deadline_cycles, uint32_t* device_error, ra_stream_t stream) {
+  using namespace ra;
+  clear_error();
+  RA_REQUIRE(deadline_cycles > 0 && deadline_cycles <= (int64_t(1) << 32), "deadline_cycles must be in (0, 2^32]");
+  RA_REQUIRE(device_error && aligned4(device_error), "device_error must be a non-null, 4-byte aligned pointer");
+  selftest_bounded_wait_kernel<<<1, 64, 0, reinterpret_cast<cudaStream_t>(stream)>>>(deadline_cycles, device_error);
+  return check_launch("selftest_bounded_wait_kernel");
+}

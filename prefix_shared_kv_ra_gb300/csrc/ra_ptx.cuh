@@ -54,12 +54,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false on deadline.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false once `deadline` SM cycles have passed.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long deadline = kWaitDeadlineCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitDeadlineCycles) return false;
+    if (clock64() - t0 > deadline) return false;
   }
   return true;
 }
@@ -88,11 +88,12 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 
 // Wait until *ctr >= target, polling with relaxed loads (follow with fence_acq_rel_gpu); false on
 // deadline.  The counter is written by other CTAs of this grid or of a grid already resident.
-__device__ __forceinline__ bool wait_count(const int32_t* ctr, int32_t target) {
+__device__ __forceinline__ bool wait_count(const int32_t* ctr, int32_t target,
+                                           long long deadline = kWaitDeadlineCycles) {
   if (ld_relaxed_gpu(ctr) >= target) return true;
   const long long t0 = clock64();
   while (ld_relaxed_gpu(ctr) < target) {
-    if (clock64() - t0 > kWaitDeadlineCycles) return false;
+    if (clock64() - t0 > deadline) return false;
     __nanosleep(256);
   }
   return true;

@@ -44,7 +44,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert ra.ra_abi_version() == 4
+    assert ra.ra_abi_version() == 5
     assert lib.ra_status_string(0) == b"ok"
     assert lib.ra_status_string(3) == b"workspace too small"
 
@@ -171,3 +171,11 @@ def test_store_decode_binding_checks_shapes_before_the_call():
         ra.ra_decode_attention_store(pool, pool, kn, kn, idx[:1], q, q.clone(), table, idx, idx, **args)
     with pytest.raises(TypeError):  # slots are int32
         ra.ra_decode_attention_store(pool, pool, kn, kn, idx.long(), q, q.clone(), table, idx, idx, **args)
+
+
+def test_selftest_bounded_wait_validates_before_launch(lib):
+    """Bad arguments are rejected on the host (nothing is launched, no GPU needed)."""
+    assert lib.ra_selftest_bounded_wait(0, FAKE, None) == 1
+    assert lib.ra_selftest_bounded_wait((1 << 32) + 1, FAKE, None) == 1
+    assert lib.ra_selftest_bounded_wait(1000, None, None) == 1
+    assert lib.ra_selftest_bounded_wait(1000, ctypes.c_void_p((1 << 20) + 2), None) == 1
