@@ -36,8 +36,8 @@ METRIC = "attn tokens/s; decode KV GB/s and extend TFLOP/s as % of GB300 rooflin
 UNIT = "tokens/s"
 WORKLOAD = ("multi-turn chat mix, 70B heads (64 q / 8 kv, head_dim 128, bf16): 256 requests, lognormal "
             "contexts (median 2048, clipped 16..32768), radix-tree prefix sharing at 70% token hit ratio; "
-            "32 extend (suffix 64..512) + 224 decode in the tree's depth-first order (cascade groups from the radix "
-            "tree); pool 2M slots")
+            "32 extend (suffix 64..512) + 224 decode in the tree's depth-first order (cascade groups of >= 4 "
+            "members from the radix tree); pool 2M slots")
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -214,21 +214,26 @@ def schedule_decode_dfs(b):
 
 def mix_step_batch(seed: int = 5):
     """The benchmark's batch: the multi-turn mix with its decode requests in the tree's depth-first order
-    and the one-level cascade groups the tree derives from them."""
+    and the one-level cascade groups the tree derives from them (at least 4 members sharing >= 256
+    tokens: with the depth-first order, smaller groups' shared slots are cheaper to read through L2 in the
+    plain decode than to run through the tensor-core prefix pass -- decode call 217 / 216 / 214 / 216 us
+    for groups of >= 2 / 3 / 4 / 6 members, same box)."""
     import workloads as W
-    return with_tree_groups(schedule_decode_dfs(W.multiturn_mix_70b(seed=seed)))
+    return with_tree_groups(schedule_decode_dfs(W.multiturn_mix_70b(seed=seed)), min_members=4)
 
 
-def with_tree_groups(b, min_prefix: int = 256, multilevel: bool = False):
+def with_tree_groups(b, min_prefix: int = 256, multilevel: bool = False, min_members: int = 2):
     """Attach the cascade groups the radix tree derives from the batch's decode table rows: one level
-    (per subtree of the root, prefixes of >= min_prefix tokens) or one group per shared node."""
+    (per subtree of the root, >= min_members requests sharing >= min_prefix tokens) or one group per
+    shared node."""
     from prefix_shared_kv_ra_gb300.radix import cascade_groups, cascade_groups_multilevel
     rows = [b.req_to_token[r, :L] for r, L in zip(b.dec_rpi, b.dec_seq_lens)]
     if multilevel:
         (b.casc_group_indptr, b.casc_group_reqs, b.casc_group_start, b.casc_group_prefix_len, b.casc_group_level,
-         b.casc_levels) = cascade_groups_multilevel(rows, min_range=min_prefix)
+         b.casc_levels) = cascade_groups_multilevel(rows, min_members=min_members, min_range=min_prefix)
     else:
-        b.casc_group_indptr, b.casc_group_reqs, b.casc_group_prefix_len = cascade_groups(rows, min_prefix=min_prefix)
+        b.casc_group_indptr, b.casc_group_reqs, b.casc_group_prefix_len = cascade_groups(
+            rows, min_prefix=min_prefix, min_members=min_members)
         b.casc_group_start, b.casc_group_level, b.casc_levels = None, None, 1
     return b
 
