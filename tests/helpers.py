@@ -147,6 +147,20 @@ def grow_key_scale(b: W.Batch, per_tile: float = 6.0, tile: int = 128) -> W.Batc
     """Scale every key by 1 + per_tile * (its context position // tile), in place: scores then grow from
     one 128-key tile to the next by far more than any lazy softmax reference allows, so kernels that
     exponentiate against a running reference must move it (and rescale O) on every tile."""
+    return scale_keys(b, lambda p: 1.0 + per_tile * (p // tile))
+
+
+def late_half_key_scale(b: W.Batch, per_tile: float = 20.0) -> W.Batch:
+    """Scale the keys at positions 64..127 of every 128-position tile by 1 + per_tile * (tile + 1) and
+    leave the others, in place.  A key tile's first 64 scores then stay within the reference of the
+    tile before while its last 64 exceed it by far: a kernel that hands out the first half's
+    probabilities before it has seen the second half must move the reference (and rescale O) between
+    the two halves of every tile."""
+    return scale_keys(b, lambda p: 1.0 + per_tile * (p // 128 + 1) if p % 128 >= 64 else 1.0)
+
+
+def scale_keys(b: W.Batch, factor) -> W.Batch:
+    """Multiply every key of the pool and of the new rows by factor(its context position), in place."""
     pos = {}
     rows = [(r, int(n)) for r, n in zip(b.ext_rpi, b.ext_prefix_lens + b.ext_extend_lens)] + \
            [(r, int(n)) for r, n in zip(b.dec_rpi, b.dec_seq_lens)]
@@ -155,7 +169,7 @@ def grow_key_scale(b: W.Batch, per_tile: float = 6.0, tile: int = 128) -> W.Batc
             pos[s] = p
 
     def scaled(bits: np.ndarray, slots: np.ndarray) -> np.ndarray:
-        f = np.array([1.0 + per_tile * (pos.get(int(s), 0) // tile) for s in slots], dtype=np.float32)
+        f = np.array([factor(pos.get(int(s), 0)) for s in slots], dtype=np.float32)
         x = W.bf16_bits_to_f32(bits) * f[:, None, None]
         return W.f32_to_bf16_bits(x)
 

@@ -8,6 +8,7 @@ import oracle
 import prefix_shared_kv_ra_gb300 as ra
 import workloads as W
 from helpers import (DeviceBatch, assert_close, attach_tree_groups, attach_tree_groups_multilevel, grow_key_scale,
+                     late_half_key_scale,
                      prefill_chunks, to_f64)
 
 pytestmark = pytest.mark.gpu
@@ -71,6 +72,18 @@ def test_extend_growing_scores(seed, hq, hkv, d):
     single-pass acceptance bound and is redone with the exact maximum and an O rescale."""
     b = grow_key_scale(W.random_mixed(seed, n_extend=5, n_decode=0, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
                                       max_len=700, min_len=300))
+    db = DeviceBatch(b)
+    db.store()
+    check_extend(db)
+
+
+@pytest.mark.parametrize("seed,hq,hkv,d", [(23, 32, 8, 128), (24, 16, 2, 64)])
+def test_extend_late_half_scores(seed, hq, hkv, d):
+    """Every key tile's last 64 scores far above its first 64 (which stay within the reference of the
+    tile before): the second half of each tile's probabilities needs a reference move after the first
+    half has gone to the PV."""
+    b = late_half_key_scale(W.random_mixed(seed, n_extend=5, n_decode=0, num_q_heads=hq, num_kv_heads=hkv,
+                                           head_dim=d, max_len=700, min_len=300))
     db = DeviceBatch(b)
     db.store()
     check_extend(db)
@@ -218,6 +231,15 @@ def test_cascade_member_without_private_keys():
 def test_cascade_growing_scores():
     """The prefix pass's tiles (several per split) under scores that grow tile by tile."""
     b = grow_key_scale(W.decode_8b_system_prompts())  # 8 groups sharing 1024 prompt tokens: 512-key splits of 4 tiles
+    assert b.has_cascade()
+    db = DeviceBatch(b)
+    db.store()
+    check_cascade(db)
+
+
+def test_cascade_late_half_scores():
+    """The prefix pass under scores whose last 64 of every key tile exceed the first 64's reference."""
+    b = late_half_key_scale(W.decode_8b_system_prompts())
     assert b.has_cascade()
     db = DeviceBatch(b)
     db.store()
