@@ -47,6 +47,7 @@ constexpr int kSmemLimit = 227 * 1024;
 constexpr int kPlanThreads = 1024;  // one CTA plans the call
 constexpr int kRemBuckets = 64;     // size classes of the requests' last (short) items
 constexpr int kCombineWarps = 4;    // (request, q head) merges per combine CTA
+constexpr float kDecodeRescale = 8.0f;  // log2 units: the decode softmax's reference moves past this
 
 // One work item: keys [k0, k1) of request b for the kv heads of head group hg; d is its dense index
 // (request-major: the item's partial results live at d).
@@ -326,27 +327,36 @@ __global__ void __launch_bounds__(32 * (kMaxHeadsPerCta + kProducers + 1), 1) de
       const float x1 = v_lo ? (s1[1] + s2[1]) * p.scale_log2 : -INFINITY;
       const float x2 = v_hi ? (s1[2] + s2[2]) * p.scale_log2 : -INFINITY;
       const float x3 = v_hi ? (s1[3] + s2[3]) * p.scale_log2 : -INFINITY;
-      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+      // Lazy reference: the running maximum moves (and O and l are rescaled) only when a score of the slab
+      // exceeds it by more than kDecodeRescale, which a warp vote finds; otherwise the slab is exponentiated
+      // against the reference as it stands (every p <= 2^kDecodeRescale).  The first slab of an item always
+      // moves it (the reference starts at -inf).
+      if (__any_sync(0xffffffffu, x0 > m0 + kDecodeRescale || x2 > m0 + kDecodeRescale ||
+                                      x1 > m1 + kDecodeRescale || x3 > m1 + kDecodeRescale)) {
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      // key 0 of a slab is always in range, so the new maxima are finite
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1), p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
-      l0 = l0 * al0 + p0 + p2;
-      l1 = l1 * al1 + p1 + p3;
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        // key 0 of a slab is always in range, so the new maxima are finite
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        l0 *= al0;
+        l1 *= al1;
 #pragma unroll
-      for (int mt = 0; mt < KT; ++mt) {
-        acc[mt][0] *= al0;
-        acc[mt][1] *= al1;
-        acc[mt][2] *= al0;
-        acc[mt][3] *= al1;
+        for (int mt = 0; mt < KT; ++mt) {
+          acc[mt][0] *= al0;
+          acc[mt][1] *= al1;
+          acc[mt][2] *= al0;
+          acc[mt][3] *= al1;
+        }
       }
+      const float p0 = ex2(x0 - m0), p1 = ex2(x1 - m1), p2 = ex2(x2 - m0), p3 = ex2(x3 - m1);
+      l0 += p0 + p2;
+      l1 += p1 + p3;
       // P^T as the B operand: transpose the two 8x8 key blocks
       const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
       const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
