@@ -7,7 +7,7 @@ import torch
 import oracle
 import prefix_shared_kv_ra_gb300 as ra
 import workloads as W
-from helpers import DeviceBatch, assert_close, bf16, i32, to_f64
+from helpers import DeviceBatch, assert_close, bf16, grow_key_scale, i32, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -73,6 +73,18 @@ def test_decode_tiny_config():
 def test_decode_ragged(seed, hq, hkv, d, max_len):
     b = W.random_mixed(seed, n_extend=0, n_decode=9, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
                        max_len=max_len)
+    db = DeviceBatch(b)
+    db.store()
+    check_decode(db)
+
+
+@pytest.mark.parametrize("seed,hq,hkv,d,per_tile", [(7, 32, 8, 128, 6.0), (8, 8, 2, 64, 0.5)])
+def test_decode_growing_scores_per_slab(seed, hq, hkv, d, per_tile):
+    """Keys scaled by 1 + per_tile * (position // 16): every 16-key slab's scores grow past the decode
+    softmax's running reference (by far, or -- with the small factor -- by amounts around its 2^8
+    rescale threshold), so its rescale of O and l runs on most slabs."""
+    b = grow_key_scale(W.random_mixed(seed, n_extend=0, n_decode=12, num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                                      min_len=200, max_len=1500), per_tile=per_tile, tile=16)
     db = DeviceBatch(b)
     db.store()
     check_decode(db)
