@@ -496,11 +496,13 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         tc_fence_after();
       }
       if (lane == 0) {
+        // descriptors built once per tile; a K step adds its byte offset / 16 to the start-address field
+        // (14 bits: shared-memory addresses / 16 stay below 2^14, so the add never carries out of it)
+        const uint64_t qd = sdesc_sw128(sQ(i), 16, 1024), kd = sdesc_sw128(sK(st), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16 && live; ++kk) {
-          const uint32_t off = (kk >> 2) * (kRows * 128) + (kk & 3) * 32;
-          tc_mma_ss(tmem + i * kKeys, sdesc_sw128(sQ(i) + off, 16, 1024), sdesc_sw128(sK(st) + off, 16, 1024),
-                    idesc_qk, kk > 0);
+          const uint32_t off16 = ((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4;
+          tc_mma_ss(tmem + i * kKeys, qd + off16, kd + off16, idesc_qk, kk > 0);
         }
         tc_commit(smem_u32(&bar_s[i]));
       }
@@ -524,10 +526,11 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       }
       if (lane == 0) {
         const bool live = i < jb.tiles;  // an empty query tile issues no PV (its O is never read)
+        const uint64_t vd = sdesc_sw128(sV(st), kRows * 128, 1024);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16 && live; ++kk) {
-          tc_mma_ts(tmem + kColO + i * 128, tmem + i * kKeys + kk * 8,
-                    sdesc_sw128(sV(st) + kk * 2048, kRows * 128, 1024), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + kColO + i * 128, tmem + i * kKeys + kk * 8, vd + kk * (2048 >> 4), idesc_pv,
+                    (j > 0 || kk > 0) ? 1u : 0u);
         }
         // Each commit stalls the tensor pipe briefly, so there are three per key tile: S_0, S_1 and the
         // K/V release here.  O_i needs none until the item's last tile: S_i's commit also covers PV_i.
