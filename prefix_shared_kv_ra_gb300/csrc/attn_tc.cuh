@@ -553,11 +553,6 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     };
     // The key tiles of consecutive items form one stream: per tile PV_0, QK_0', PV_1, QK_1', where the
     // QKs after an item's last tile are the next item's first.
-    auto qk_first = [&](int i, int gg) -> bool {  // item n+1's first QK on tile i
-      if (!wait_all(bar_q[i], (n + 1) & 1)) return false;
-      tc_fence_after();
-      return qk(i, gg, i < jn.tiles);
-    };
     if (ok && r > 0) {
       ok = wait_all(bar_q[0], 0) && wait_all(bar_q[1], 0);
       if (ok) {
@@ -569,12 +564,23 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       for (int j = 0; ok && j < jb.nt; ++j) {
         if (aborted(abort_flag)) { ok = false; break; }
         const int gg = g + j;
-        if (j + 1 < jb.nt) {
-          ok = pv(0, gg, j) && qk(0, gg + 1, true) && pv(1, gg, j) && qk(1, gg + 1, jb.tiles > 1);
-        } else {
-          ok = reload_q(0, gg) && pv(0, gg, j) && reload_q(1, gg) && (next == 0 || qk_first(0, gg + 1)) &&
-               pv(1, gg, j) && (next == 0 || qk_first(1, gg + 1));
-        }
+        const bool last = j + 1 == jb.nt;
+        // The QK on tile i after this key tile's PV: this item's next key tile, or after its last the next
+        // item's first, once that item's query tile has landed.  One call site per query tile: the loop
+        // body exists once (a copy for an item's last tile measured 6-8% slower: the MMA warp's code
+        // shares an instruction cache with the softmax warps of its sub-partition).
+        auto qk_after = [&](int i) -> bool {
+          bool live = i == 0 || jb.tiles > 1;
+          if (last) {
+            if (next == 0) return true;
+            if (!wait_all(bar_q[i], (n + 1) & 1)) return false;
+            tc_fence_after();
+            live = i < jn.tiles;
+          }
+          return qk(i, gg + 1, live);
+        };
+        ok = (!last || reload_q(0, gg)) && pv(0, gg, j) && (!last || reload_q(1, gg)) && qk_after(0) &&
+             pv(1, gg, j) && qk_after(1);
       }
       if (!ok) break;
       g += jb.nt;
