@@ -37,7 +37,8 @@
 // warp redoes the tile on the exact path (row maximum first).  O / l is exact softmax.
 //
 // Every mbarrier wait is bounded; on a timeout the CTA flags RA_DEVERR_TIMEOUT, every role
-// drains and leaves, and TMEM is freed.
+// drains and leaves (the producers at once through the CTA's abort flag, the MMA and softmax warps at
+// the deadline of their next wait), and TMEM is freed.
 #pragma once
 
 #include <cuda.h>
@@ -561,8 +562,9 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       }
     }
     while (ok && r > 0) {
+      // (no per-tile look at the abort flag: after a failure elsewhere this warp leaves through the
+      // deadline of its next wait; the check on the loop's back edge measured ~1% of the kernel)
       for (int j = 0; ok && j < jb.nt; ++j) {
-        if (aborted(abort_flag)) { ok = false; break; }
         const int gg = g + j;
         const bool last = j + 1 == jb.nt;
         // The QK on tile i after this key tile's PV: this item's next key tile, or after its last the next
@@ -616,7 +618,8 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < jb.nt; ++j) {
         const int gg = g + j;
-        const bool fail_here = aborted(abort_flag) || !mbar_wait(smem_u32(&bar_s[ti]), gg & 1);
+        // (as in the MMA warp, no per-tile look at the abort flag: the wait's deadline ends a failed CTA)
+        const bool fail_here = !mbar_wait(smem_u32(&bar_s[ti]), gg & 1);
         if (__any_sync(0xffffffffu, fail_here)) { ok = false; break; }  // warp-uniform: tcgen05.ld/st are collective
         if (ti >= jb.tiles) {  // an empty query tile: no S was computed; keep bar_p's phase
           mbar_arrive(smem_u32(&bar_p[ti]));
