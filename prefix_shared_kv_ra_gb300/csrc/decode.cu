@@ -788,7 +788,7 @@ static int32_t heads_per_cta(int32_t num_kv_heads) {
 // Shared-prefix pass (cascade): 256-row items of (member, q head) per group and kv head, each covering
 // at most `cchunk` prefix keys.  The persistent private decode is launched programmatically after it
 // and runs on the SMs the prefix pass leaves free.
-DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_seq_len,
+DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t max_seq_len,
                        int32_t num_groups, int32_t max_group_prefix_len, int32_t max_group_size) {
   DecodePlan pl;
   pl.max_items = kDecodePlanItems + batch;
@@ -811,11 +811,27 @@ DecodePlan plan_decode(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
     // host, possibly with no device current) must not depend on which device runs the call.
     const int64_t share = 152 * static_cast<int64_t>(max_group_prefix_len) / (max_seq_len > 0 ? max_seq_len : 1);
     const int64_t sms = share < 104 ? 104 : (share > 152 ? 152 : share);
-    int64_t best_tiles = 16, best_cost = -1;
+    // Batches whose contexts are the shared prefix plus a short private tail (its bound at most 1/8 of the
+    // prefix): the SMs beyond the pass decode the tails -- on average half the bound, ~105 KB per SM per
+    // key tile of the pass (~50 GB/s per SM while HBM is not saturated, measured), starting ~4 tiles
+    // after the pass -- and the split balances the two.  Measured on a forked batch (8192 shared keys,
+    // tails of 0..256): 1024 / 1280 / 1408 / 1536 / 1664 / 1792 keys per CTA took 54.2 / 49.0 / 50.6 /
+    // 52.1 / 53.1 / 56.3 us; this picks 1280.
+    const int64_t tail = static_cast<int64_t>(max_seq_len) - max_group_prefix_len;
+    const bool short_tails = tail >= 0 && 8 * tail <= max_group_prefix_len;
+    const double tail_bytes = 0.5 * static_cast<double>(batch) * static_cast<double>(tail) * num_kv_heads *
+                              static_cast<double>(head_dim) * 2 * 2;
+    int64_t best_tiles = 16;
+    double best_cost = -1.0;
     for (int64_t per = 16; per >= 1; --per) {  // tiles per CTA
       const int64_t splits = (tiles + per - 1) / per;
       const int64_t waves = (base * splits + sms - 1) / sms;
-      const int64_t cost = waves * (per + 3);
+      double cost = static_cast<double>(waves * (per + 3));
+      if (short_tails) {
+        const int64_t ctas = base * splits < sms ? base * splits : sms;
+        const double tail_cost = tail_bytes / (static_cast<double>(152 - ctas) * 105e3) + 4.0;
+        if (tail_cost > cost) cost = tail_cost;
+      }
       if (best_cost < 0 || cost < best_cost) {
         best_cost = cost;
         best_tiles = per;
@@ -865,7 +881,7 @@ extern "C" size_t ra_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, 
                                             int32_t max_group_levels) {
   if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
   if (num_groups > 0 && (max_group_prefix_len <= 0 || max_group_size <= 0 || max_group_levels <= 0)) return 0;
-  const ra::DecodePlan pl = ra::plan_decode(batch, num_q_heads, num_kv_heads, max_seq_len, num_groups,
+  const ra::DecodePlan pl = ra::plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, num_groups,
                                             max_group_prefix_len, max_group_size);
   return ra::layout_decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, pl,
                                      num_groups > 0 ? max_group_levels : 0)
@@ -924,7 +940,7 @@ static ra_status decode_call(const void* k_pool, const void* v_pool, int64_t num
   // the device plan's item length must fit in 31 bits (it is at most batch x max_seq_len / kDecodePlanItems)
   RA_REQUIRE(static_cast<int64_t>(batch) * max_seq_len <= static_cast<int64_t>(kDecodePlanItems) << 30,
              "batch x max_seq_len too large");
-  const DecodePlan pl = plan_decode(batch, num_q_heads, num_kv_heads, max_seq_len, num_groups,
+  const DecodePlan pl = plan_decode(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, num_groups,
                                     max_group_prefix_len, max_group_size);
   const int32_t levels = num_groups > 0 ? max_group_levels : 0;
   const DecodeWorkspace wl = layout_decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, pl, levels);
