@@ -448,6 +448,11 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
     if (lane == 0) prefetch_tensormap(&qmap);
     constexpr uint32_t idesc_qk = idesc_bf16_f32(kRows, kKeys, 0, 0);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(kRows, D, 0, 1);
+    // Every Q, K and V tile sits at a fixed shared-memory offset: one descriptor per operand kind, a
+    // tile's and a K step's offsets added to its start-address field (addresses / 16 stay below 2^14).
+    const uint64_t desc_q0 = sdesc_sw128(sQ(0), 16, 1024), desc_k0 = sdesc_sw128(sK(0), 16, 1024);
+    const uint64_t desc_v0 = sdesc_sw128(sV(0), kRows * 128, 1024);
+    constexpr uint32_t kTile16 = L::kTileBytes >> 4;
     // query tile i of an extend job into sQ(i): one 3-D TMA tile load per 64-column half (the K warps
     // gather the prefix pass's member rows)
     auto load_q = [&](const Job& jb, int i) {
@@ -497,9 +502,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
         tc_fence_after();
       }
       if (lane == 0) {
-        // descriptors built once per tile; a K step adds its byte offset / 16 to the start-address field
-        // (14 bits: shared-memory addresses / 16 stay below 2^14, so the add never carries out of it)
-        const uint64_t qd = sdesc_sw128(sQ(i), 16, 1024), kd = sdesc_sw128(sK(st), 16, 1024);
+        const uint64_t qd = desc_q0 + i * kTile16, kd = desc_k0 + st * kTile16;
 #pragma unroll
         for (int kk = 0; kk < D / 16 && live; ++kk) {
           const uint32_t off16 = ((kk >> 2) * (kRows * 128) + (kk & 3) * 32) >> 4;
@@ -527,7 +530,7 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
       }
       if (lane == 0) {
         const bool live = i < jb.tiles;  // an empty query tile issues no PV (its O is never read)
-        const uint64_t vd = sdesc_sw128(sV(st), kRows * 128, 1024);
+        const uint64_t vd = desc_v0 + st * kTile16;
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16 && live; ++kk) {
           tc_mma_ts(tmem + kColO + i * 128, tmem + i * kKeys + kk * 8, vd + kk * (2048 >> 4), idesc_pv,
