@@ -179,3 +179,26 @@ def test_selftest_bounded_wait_validates_before_launch(lib):
     assert lib.ra_selftest_bounded_wait((1 << 32) + 1, FAKE, None) == 1
     assert lib.ra_selftest_bounded_wait(1000, None, None) == 1
     assert lib.ra_selftest_bounded_wait(1000, ctypes.c_void_p((1 << 20) + 2), None) == 1
+
+
+def _decode_workspace_layout(batch, hq, d, csplits, levels=1):
+    """The decode workspace's size from its layout: per-item partials, prefix partials, the integer block."""
+    up = lambda x: (x + 255) & ~255
+    max_items = 456 + batch
+    total = up(max_items * hq * d * 4) + up(max_items * hq * 4)
+    if csplits:
+        slots = levels * csplits
+        total += up(batch * hq * slots * d * 4) + up(batch * hq * slots * 4)
+    return total + up((batch + 3) * 4 + (2 + batch + 1 + 2 * max_items + batch) * 4)
+
+
+def test_decode_prefix_split_balances_short_private_tails(lib):
+    """The prefix pass's split, seen through the workspace size (one partial slot per split): a batch whose
+    contexts are one 8192-key prefix plus tails of at most 257 keys gets 1,280-key splits (7), balanced
+    against the tails' decode on the SMs the pass leaves free; a batch with long private parts keeps the
+    split that fills the pass's wave (one 1,024-key split of its 1,024-key prefix)."""
+    assert ra.ra_decode_workspace_bytes(64, 64, 8, 128, 8449, 1, 8192, 64, 1) == \
+        _decode_workspace_layout(64, 64, 128, csplits=7)
+    assert ra.ra_decode_workspace_bytes(64, 32, 8, 128, 4096, 8, 1024, 8, 1) == \
+        _decode_workspace_layout(64, 32, 128, csplits=1)
+    assert ra.ra_decode_workspace_bytes(64, 32, 8, 128, 4096) == _decode_workspace_layout(64, 32, 128, csplits=0)
